@@ -1,0 +1,258 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks the oracle against a hand-worked example, brute force, a
+library routine that implements the same definition (PyTorch's GRUCell and
+SiLU), a closed form, or an invariant the pages state (first proposal is the
+uncorrected full-vocabulary argmax; K=0 / full pool are the exact search).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_draft_lm_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked_rollout.json")
+
+
+def _golden_case(case, common):
+    w = {k: np.asarray(v, dtype=np.float32) for k, v in common.items()}
+    w["emb"] = np.asarray(case["emb"], dtype=np.float32)
+    return w
+
+
+def golden_cases():
+    with open(GOLDEN) as f:
+        g = json.load(f)
+    req = {
+        "hidden": np.asarray(g["hidden"], dtype=np.float32).reshape(1, 16, 1),
+        "s": np.asarray(g["s"], dtype=np.float32).reshape(1, 15, 1),
+    }
+    for case in g["cases"]:
+        r = dict(req)
+        r["verified"] = np.asarray([case["verified"]], dtype=np.int32)
+        yield case, _golden_case(case, g["weights_common"]), r
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2])
+def test_hand_worked_golden(idx):
+    case, w, r = list(golden_cases())[idx]
+    out = oracle.run(w, r, K=case["K"])
+    assert out["tokens"][0].tolist() == case["expected"], case["name"]
+
+
+def test_golden_alternative_readings_differ():
+    """The hand-worked tokens change under the plausible mistakes they guard."""
+    case, w, r = list(golden_cases())[0]
+    good = oracle.run(w, r, K=0)["tokens"][0].tolist()
+    # swapped seed order: feed p1 first, then the verified token
+    W = oracle.OracleWeights(w)
+    h = oracle.gru_cell(W.emb[[1]], np.zeros((1, 1)), W.w_ih, W.w_hh)
+    h = oracle.gru_cell(W.emb[[2]], h, W.w_ih, W.w_hh)
+    z = h @ W.fc1.T + oracle.widen(r["s"])[:, 1]
+    L2 = oracle.lm_head(r["hidden"], w["lm_head"])[0, 2]
+    c = W.fc2 @ oracle.silu(z[0]) + W.b + L2
+    assert oracle.argmax_lowest(c) != good[1]
+
+
+def test_widen_bf16_bits_exact():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x3F81, 0x7F7F, 0x0001], dtype=np.uint16)
+    want = [1.0, -2.0, 0.0, -0.0, 1.0 + 2.0 ** -7, (2 - 2.0 ** -7) * 2.0 ** 127, 2.0 ** -133]
+    got = oracle.widen(bits)
+    assert got.dtype == np.float64
+    assert got.tolist() == want
+
+
+def test_generator_bf16_rounding_is_nearest_even():
+    # 1 + 2^-8 is halfway between bf16 1.0 and 1+2^-7 -> even (1.0);
+    # 1 + 3*2^-8 is halfway between 1+2^-7 and 1+2^-6 -> even (1+2^-6)
+    x = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -8 + 2 ** -20, -1.5], dtype=np.float32)
+    got = oracle.widen(inputs.to_bf16_bits(x)).tolist()
+    assert got == [1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -1.5]
+
+
+def test_lm_head_matches_bruteforce_loops():
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((2, 16, 7)).astype(np.float32)
+    W = rng.standard_normal((11, 7)).astype(np.float32)
+    L = oracle.lm_head(X, W, chunk=4)
+    for b, i, v in itertools.product(range(2), range(16), range(11)):
+        acc = 0.0
+        for h in range(7):
+            acc += float(X[b, i, h]) * float(W[v, h])
+        assert abs(L[b, i, v] - acc) < 1e-12
+
+
+def test_argmax_lowest_index_on_ties_and_bruteforce():
+    assert oracle.argmax_lowest(np.array([1.0, 3.0, 3.0, 2.0])) == 1
+    assert oracle.argmax_lowest(np.array([0.0, -0.0, 0.0])) == 0
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        c = rng.integers(-3, 4, size=17).astype(np.float64)
+        best = 0
+        for j in range(1, 17):
+            if c[j] > c[best]:
+                best = j
+        assert oracle.argmax_lowest(c) == best
+        srt = sorted(c.tolist(), reverse=True)
+        assert oracle.top2_margin(c) == srt[0] - srt[1]
+
+
+def test_gru_cell_matches_torch_grucell():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(2)
+    E, G, B = 6, 5, 3
+    w_ih = rng.standard_normal((3 * G, E))
+    w_hh = rng.standard_normal((3 * G, G))
+    x = rng.standard_normal((B, E))
+    h = rng.standard_normal((B, G))
+    cell = torch.nn.GRUCell(E, G, bias=False).double()
+    with torch.no_grad():
+        cell.weight_ih.copy_(torch.from_numpy(w_ih))
+        cell.weight_hh.copy_(torch.from_numpy(w_hh))
+        want = cell(torch.from_numpy(x), torch.from_numpy(h)).numpy()
+    got = oracle.gru_cell(x, h, w_ih, w_hh)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-13)
+
+
+def test_gru_closed_forms():
+    rng = np.random.default_rng(3)
+    E, G = 4, 3
+    w_ih = rng.standard_normal((3 * G, E))
+    x = rng.standard_normal(E)
+    # W_hh = 0 and h = 0: h' = (1 - sigmoid(W_iz x)) * tanh(W_in x)
+    got = oracle.gru_cell(x, np.zeros(G), w_ih, np.zeros((3 * G, G)))
+    wz = w_ih[G:2 * G] @ x
+    wn = w_ih[2 * G:] @ x
+    want = [(1 - 1 / (1 + math.exp(-wz[j]))) * math.tanh(wn[j]) for j in range(G)]
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+    # all weights zero: r = u = 1/2, n = 0, so h' = h / 2
+    h = rng.standard_normal(G)
+    got = oracle.gru_cell(x, h, np.zeros((3 * G, E)), np.zeros((3 * G, G)))
+    np.testing.assert_allclose(got, h / 2, rtol=0, atol=0)
+
+
+def test_silu_matches_torch():
+    torch = pytest.importorskip("torch")
+    z = np.linspace(-30, 30, 1001)
+    want = torch.nn.functional.silu(torch.from_numpy(z)).numpy()
+    np.testing.assert_allclose(oracle.silu(z), want, rtol=1e-15, atol=1e-300)
+
+
+def test_candidate_pool_matches_sorted_bruteforce():
+    rng = np.random.default_rng(4)
+    for K in (1, 5, 9, 20):
+        rows = rng.integers(-4, 5, size=(15, 23)).astype(np.float64)  # many ties
+        score = rows.max(axis=0)
+        ranked = sorted(range(23), key=lambda v: (-score[v], v))
+        want = sorted(ranked[:K]) if K < 23 else list(range(23))
+        assert oracle.candidate_pool(rows, K).tolist() == want
+    assert oracle.candidate_pool(rows, 0).tolist() == list(range(23))
+    assert oracle.candidate_pool(rows, 23).tolist() == list(range(23))
+
+
+# ---- invariants on a small random workload --------------------------------
+
+SMALL = inputs.small_shape(V=300, H=24, E=12, G=16, F=20, dtype="fp32")
+
+
+def _small(B=3, seed=7, scales=None):
+    # emb ~ N(0,1) and GRU ~ N(0,1/sqrt(E)) so that the feedback path moves tokens
+    sc = {"emb": 1.0, "w_ih": 12 ** -0.5, "w_hh": 16 ** -0.5, "fc1": 0.3, "fc2": 1.0}
+    sc.update(scales or {})
+    w = inputs.make_weights(SMALL, seed=seed, scales=sc)
+    r = inputs.make_requests(SMALL, list(range(10, 10 + B)))
+    return w, r
+
+
+def test_first_proposal_is_uncorrected_argmax():
+    w, r = _small()
+    out = oracle.run(w, r)
+    for b in range(3):
+        assert out["tokens"][b, 0] == int(np.argmax(out["L"][b, 1]))
+
+
+def test_full_pool_equals_k0():
+    w, r = _small()
+    a = oracle.run(w, r, K=0)
+    b = oracle.run(w, r, K=SMALL.V)
+    assert (a["tokens"] == b["tokens"]).all()
+
+
+def test_zero_correction_gives_base_argmax_chain():
+    w, r = _small()
+    w["fc2"][:] = 0
+    w["b"][:] = 0
+    out = oracle.run(w, r)
+    for b in range(3):
+        want = [int(np.argmax(out["L"][b, j + 1])) for j in range(15)]
+        assert out["tokens"][b].tolist() == want
+
+
+def test_bias_mutation_forces_every_corrected_step():
+    w, r = _small()
+    vstar = 123
+    w["b"][vstar] = 1e3
+    out = oracle.run(w, r)
+    assert (out["tokens"][:, 1:] == vstar).all()
+    # and in pool mode when v* is in the pool (its score ties nothing)
+    outk = oracle.run(w, r, K=50)
+    for b in range(3):
+        if vstar in outk["pool"][b]:
+            assert (outk["tokens"][b, 1:] == vstar).all()
+        else:
+            assert (outk["tokens"][b, 1:] != vstar).all()
+
+
+def test_feedback_path_changes_tokens():
+    """With the scaled weights the GRU state matters (guards a dead feedback)."""
+    w, r = _small()
+    out = oracle.run(w, r)
+    forced = out["tokens"].copy()
+    forced[:, :] = (forced + 1) % SMALL.V
+    tf = oracle.run(w, r, forced=forced)
+    assert not np.allclose(tf["h"][:, 1:], out["h"][:, 1:])
+    # teacher forcing with the rollout's own chain reproduces it exactly
+    same = oracle.run(w, r, forced=out["tokens"])
+    assert (same["tokens"] == out["tokens"]).all()
+    np.testing.assert_array_equal(same["h"], out["h"])
+
+
+@pytest.mark.parametrize("K", [0, 40])
+def test_vocab_permutation_permutes_tokens(K):
+    w, r = _small()
+    perm = np.random.default_rng(9).permutation(SMALL.V)  # new id of old id
+    inv = np.argsort(perm)
+    wp = dict(w)
+    for n in ("lm_head", "emb", "fc2", "b"):
+        wp[n] = w[n][inv]
+    rp = dict(r)
+    rp["verified"] = perm[r["verified"]].astype(np.int32)
+    a = oracle.run(w, r, K=K)
+    b = oracle.run(wp, rp, K=K)
+    assert (perm[a["tokens"]] == b["tokens"]).all()
+
+
+@pytest.mark.parametrize("K", [0, 40])
+def test_batch_independence(K):
+    w, r = _small(B=4)
+    whole = oracle.run(w, r, K=K)
+    for b in range(4):
+        one = {k: v[b:b + 1] for k, v in r.items()}
+        single = oracle.run(w, one, K=K)
+        assert (single["tokens"][0] == whole["tokens"][b]).all()
+        np.testing.assert_allclose(single["h"][0], whole["h"][b], rtol=0, atol=1e-12)
+
+
+def test_step_count_and_shapes():
+    w, r = _small(B=2)
+    out = oracle.run(w, r, K=40, keep_scores=True)
+    assert out["tokens"].shape == (2, 15)
+    assert out["h"].shape == (2, 15, SMALL.G)
+    assert out["z"].shape == (2, 14, SMALL.F)
+    assert out["c"][0].shape == (14, 40)
+    assert all(len(p) == 40 and (np.diff(p) > 0).all() for p in out["pool"])
