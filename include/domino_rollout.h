@@ -1,0 +1,170 @@
+/*
+ * domino_rollout.h - C ABI of the GB300 (sm_103a) Domino draft-block rollout.
+ *
+ * The operation (page "Add correctness-first Domino support to DFlash V2",
+ * section "Design"; page "[Spec] Add Domino projector support to DFlash
+ * speculative decoding (V2)", section "Implementation"): for each of B
+ * independent requests, given the 16 draft hidden states of a DFlash block,
+ *
+ *   1. base logits  L[b,i,:] = lm_head @ hidden[b,i,:]  for the 16 rows i;
+ *   2. p_1 = argmax of base row 1 over the full vocabulary (uncorrected);
+ *   3. a bias-free GRU (gate rows r|z|n, h_0 = 0) is seeded with the
+ *      embeddings of [verified_token, p_1];
+ *   4. for corrected step k = 1..14:
+ *        a = SiLU(fc1 @ h + s[b,k,:]),
+ *        c[v] = fc2[v,:] . a + bias[v] + L[b,k+1,v]   (v in the pool),
+ *        p_{k+1} = argmax_v c[v]  (lowest token id on ties),
+ *        and, for k < 14, h = GRU(emb[p_{k+1}], h);
+ *   5. out_tokens[b,:] = [p_1 .. p_15].
+ *
+ * The pool (page "Add correctness-first Domino support to DFlash V2",
+ * section "Design": one per-request, block-shared candidate pool; size 0
+ * means the full vocabulary) is, for 0 < K < V, the K token ids with the
+ * largest max over base rows 1..15 (ties to the lower id).  K = 0 or K >= V
+ * scores the full vocabulary.
+ *
+ * Threading: a context may be used from one host thread at a time.  All
+ * calls taking a stream are asynchronous on that stream and make no host
+ * synchronisation, except domino_rollout_status().  Every entry point
+ * returns DOMINO_OK (0) or a negative status; nothing falls back to the CPU.
+ */
+#ifndef DOMINO_ROLLOUT_H
+#define DOMINO_ROLLOUT_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DOMINO_API __attribute__((visibility("default")))
+#else
+#define DOMINO_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define DOMINO_OK                 0
+#define DOMINO_ERR_INVALID_ARG   -1  /* null pointer, B > max_B, K < 0, bad size   */
+#define DOMINO_ERR_UNSUPPORTED   -2  /* block != 16, unknown dtype, misaligned dims */
+#define DOMINO_ERR_NOT_LOADED    -3  /* run before load_weights                      */
+#define DOMINO_ERR_CUDA          -4  /* a CUDA call or launch failed                 */
+#define DOMINO_ERR_OOM           -5  /* workspace allocation failed                  */
+#define DOMINO_ERR_TIMEOUT       -6  /* a device-side wait hit its iteration limit   */
+#define DOMINO_ERR_BAD_TOKEN     -7  /* verified/forced token outside [0, V)         */
+
+#define DOMINO_DTYPE_FP32 0  /* fp32 weights/activations, fp32 arithmetic          */
+#define DOMINO_DTYPE_BF16 1  /* bf16 weights/activations, fp32 accumulation        */
+
+#define DOMINO_BLOCK 16      /* draft block size; 15 proposals per request         */
+
+typedef struct domino_ctx domino_ctx;
+
+/* Model dimensions fixed at init.  V vocabulary, H draft hidden size, E token
+ * embedding size, G GRU state size, F projector width (fc1 rows, fc2 cols).
+ * For DOMINO_DTYPE_BF16, H, E, G and F must be multiples of 8 (16-byte rows
+ * for the bulk copies).  max_B / max_K size the workspace. */
+typedef struct {
+    int V, H, E, G, F;
+    int block;   /* must be DOMINO_BLOCK */
+    int max_B;   /* largest batch passed to run(), >= 1 */
+    int max_K;   /* largest pool size passed to run() (0: full vocabulary only) */
+    int dtype;   /* DOMINO_DTYPE_* */
+} domino_config;
+
+/* Create a context on CUDA device `device` and allocate its workspace there:
+ * base logits [max_B,16,V] fp32, pool scores [max_B,V], pool [max_B,max_K],
+ * GRU/projector state and the per-step argmax words.  *out receives the
+ * context (NULL on failure).  Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM. */
+DOMINO_API int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device);
+
+/* Register the weights: DEVICE pointers, row-major, in the config's dtype,
+ * BORROWED (the caller keeps them alive and unchanged until destroy or the
+ * next load_weights).  Shapes: lm_head [V,H]; emb [V,E]; w_ih [3G,E] and
+ * w_hh [3G,G] with gate rows r|z|n; fc1 [F,G]; fc2 [V,F]; bias [V].
+ * Pointers must be 16-byte aligned.  Builds the TMA descriptors; no copy.
+ * Errors: INVALID_ARG, CUDA. */
+DOMINO_API int domino_rollout_load_weights(domino_ctx* ctx, const void* lm_head, const void* emb,
+                                const void* w_ih, const void* w_hh, const void* fc1,
+                                const void* fc2, const void* bias);
+
+/* Run one block rollout for B requests on `cuda_stream` (a cudaStream_t,
+ * NULL = legacy default stream).  DEVICE pointers, owned by the caller:
+ *   hidden       [B,16,H]  draft hidden states (config dtype, 16-B aligned)
+ *   s            [B,15,F]  per-step additive term of projector layer 1
+ *                          (row 0 is not read; row k serves corrected step k)
+ *   verified_tok [B] int32 the block's verified token
+ *   out_tokens   [B,15] int32 proposals p_1..p_15 (written)
+ * K: pool size; 0 (or >= V) = full-vocabulary correction; 0 < K < V needs
+ * K <= max_K.  A verified token outside [0,V) is caught on the device: that
+ * request's row of out_tokens becomes -1 and domino_rollout_status() reports
+ * DOMINO_ERR_BAD_TOKEN.  Errors returned directly: INVALID_ARG,
+ * NOT_LOADED, CUDA. */
+DOMINO_API int domino_rollout_run(domino_ctx* ctx, const void* hidden, const void* s,
+                       const int32_t* verified_tok, int B, int K,
+                       int32_t* out_tokens, void* cuda_stream);
+
+/* Optional dumps for domino_rollout_debug_run (each DEVICE pointer may be
+ * NULL, caller-owned, fp32 unless noted). */
+typedef struct {
+    float*   logits;  /* [B,16,V] base logits                                   */
+    int32_t* pool;    /* [B,K] pool ids, ascending (only when 0 < K < V)        */
+    float*   h;       /* [B,15,G] GRU state after each of the 15 updates        */
+    float*   z;       /* [B,14,F] projector pre-activation of each step         */
+    float*   top1;    /* [B,15] winning score of each proposal                  */
+    float*   scores;  /* [B,14,Kc] corrected scores, Kc = V (K0) or K (pool)    */
+} domino_debug_bufs;
+
+/* As domino_rollout_run, plus teacher forcing and dumps.  forced_tokens
+ * (nullable DEVICE [B,15] int32): when given, the GRU is fed forced[b,k]
+ * instead of p_{k+1}, while out_tokens still reports each step's own argmax.
+ * A forced token outside [0,V) is a BAD_TOKEN fault like a verified one. */
+DOMINO_API int domino_rollout_debug_run(domino_ctx* ctx, const void* hidden, const void* s,
+                             const int32_t* verified_tok, int B, int K,
+                             const int32_t* forced_tokens, const domino_debug_bufs* dbg,
+                             int32_t* out_tokens, void* cuda_stream);
+
+/* Driver of the 14 dependent steps. */
+#define DOMINO_DRIVER_AUTO       0  /* pick per (B, K)                              */
+#define DOMINO_DRIVER_KERNELS    1  /* one launch per phase, stream-ordered         */
+#define DOMINO_DRIVER_PERSISTENT 2  /* one cooperative launch with grid barriers    */
+DOMINO_API int domino_rollout_set_driver(domino_ctx* ctx, int driver);
+
+/* Per-phase timing.  When enabled, run()/debug_run() record a pair of CUDA
+ * events on the run's stream around every launch and tag it with its phase
+ * (DOMINO_PHASE_*).  read_timing() waits for the recorded events, adds each
+ * pair's elapsed time to ms[phase] and its launch to launches[phase] (both
+ * caller-owned host arrays of DOMINO_N_PHASES entries, zeroed by the caller)
+ * and forgets them.  At most 4096 pending pairs are kept; call read_timing()
+ * after each run.  Errors: INVALID_ARG, CUDA. */
+#define DOMINO_PHASE_LMHEAD     0  /* base LM-head (+ fused epilogue)                */
+#define DOMINO_PHASE_ARGMAX     1  /* first-proposal argmax                          */
+#define DOMINO_PHASE_POOL       2  /* candidate pool (score + select)                */
+#define DOMINO_PHASE_GRU        3  /* GRU updates                                    */
+#define DOMINO_PHASE_FC1        4  /* projector layer 1 + SiLU                       */
+#define DOMINO_PHASE_CORRECT    5  /* correction + argmax                            */
+#define DOMINO_PHASE_STEPS      6  /* persistent driver of the 14 steps              */
+#define DOMINO_PHASE_OTHER      7  /* reset, write-out, debug copies                 */
+#define DOMINO_N_PHASES         8
+DOMINO_API int domino_rollout_enable_timing(domino_ctx* ctx, int enable);
+DOMINO_API int domino_rollout_read_timing(domino_ctx* ctx, float* ms, int* launches);
+
+/* Synchronise `cuda_stream`, then return and clear the device error word
+ * (DOMINO_OK, DOMINO_ERR_BAD_TOKEN or DOMINO_ERR_TIMEOUT), or DOMINO_ERR_CUDA
+ * if the stream reported an error. */
+DOMINO_API int domino_rollout_status(domino_ctx* ctx, void* cuda_stream);
+
+/* Number of kernel launches the last run()/debug_run() enqueued. */
+DOMINO_API int domino_rollout_last_launch_count(const domino_ctx* ctx);
+
+/* Free the workspace and the context (NULL is ignored).  Synchronises the
+ * context's device first.  Weights stay the caller's. */
+DOMINO_API void domino_rollout_destroy(domino_ctx* ctx);
+
+/* Static description of a status code. */
+DOMINO_API const char* domino_rollout_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DOMINO_ROLLOUT_H */

@@ -1,0 +1,293 @@
+// C ABI of the Domino draft-block rollout: argument checks, workspace, the
+// sequence of launches for one block, status and teardown.
+#include <stdlib.h>
+#include <string.h>
+
+#include "internal.h"
+
+using namespace domino;
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_config(const domino_config* g) {
+    if (!g) return DOMINO_ERR_INVALID_ARG;
+    if (g->block != DOMINO_BLOCK) return DOMINO_ERR_UNSUPPORTED;
+    if (g->dtype != DOMINO_DTYPE_FP32 && g->dtype != DOMINO_DTYPE_BF16) return DOMINO_ERR_UNSUPPORTED;
+    if (g->V < 2 || g->H < 1 || g->E < 1 || g->G < 1 || g->F < 1 || g->max_B < 1 || g->max_K < 0)
+        return DOMINO_ERR_INVALID_ARG;
+    if (g->max_B > 4096) return DOMINO_ERR_INVALID_ARG;
+    if (g->dtype == DOMINO_DTYPE_BF16 && ((g->H | g->E | g->G | g->F) & 7)) return DOMINO_ERR_UNSUPPORTED;
+    return DOMINO_OK;
+}
+
+// Event pair around one launch when timing is on; returns the pair's slot
+// (-1 when off or when the pending list is full).
+int timing_begin(domino_ctx* c, cudaStream_t st, int phase) {
+    if (!c->timing || c->n_pending >= 4096) return -1;
+    int i = c->n_pending;
+    while (c->n_events < 2 * (i + 1)) {
+        if (cudaEventCreate(&c->ev[c->n_events]) != cudaSuccess) return -1;
+        ++c->n_events;
+    }
+    if (cudaEventRecord(c->ev[2 * i], st) != cudaSuccess) return -1;
+    c->pending_phase[i] = phase;
+    c->n_pending = i + 1;
+    return i;
+}
+
+cudaError_t timing_end(domino_ctx* c, cudaStream_t st, int slot) {
+    if (slot < 0) return cudaSuccess;
+    return cudaEventRecord(c->ev[2 * slot + 1], st);
+}
+
+int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* verified, int B, int K,
+             const int32_t* forced, const domino_debug_bufs* dbg, int32_t* out, void* stream) {
+    if (!c) return DOMINO_ERR_INVALID_ARG;
+    if (!c->loaded) return DOMINO_ERR_NOT_LOADED;
+    if (B < 0 || B > c->cfg.max_B || K < 0) return DOMINO_ERR_INVALID_ARG;
+    if (B == 0) {
+        c->last_launches = 0;
+        return DOMINO_OK;
+    }
+    if (!hidden || !s || !verified || !out) return DOMINO_ERR_INVALID_ARG;
+    const int Keff = (K >= c->cfg.V) ? 0 : K;
+    if (Keff > c->cfg.max_K) return DOMINO_ERR_INVALID_ARG;
+    if (c->cfg.dtype == DOMINO_DTYPE_BF16 && (!aligned16(hidden) || !aligned16(s))) return DOMINO_ERR_INVALID_ARG;
+
+    DeviceGuard guard(c->device);
+    RunArgs r;
+    memset(&r, 0, sizeof(r));
+    r.hidden = hidden;
+    r.s = s;
+    r.verified = verified;
+    r.B = B;
+    r.K = Keff;
+    r.forced = forced;
+    if (dbg) r.dbg = *dbg;
+    r.out_tokens = out;
+    r.st = (cudaStream_t)stream;
+
+    cudaError_t e;
+#define STEP(phase, x)                                   \
+    do {                                                 \
+        int slot_ = timing_begin(c, r.st, phase);        \
+        e = (x);                                         \
+        if (e != cudaSuccess) goto fail;                 \
+        e = timing_end(c, r.st, slot_);                  \
+        if (e != cudaSuccess) goto fail;                 \
+    } while (0)
+    STEP(DOMINO_PHASE_OTHER, launch_reset(c, r));
+    if (c->cfg.dtype == DOMINO_DTYPE_BF16 && lmhead_tc_supported(c))
+        STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_tc(c, r));
+    else
+        STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_simt(c, r));
+    STEP(DOMINO_PHASE_ARGMAX, launch_first_argmax(c, r));
+    if (r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, false));
+    STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 0));
+    STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 1));
+    for (int k = 1; k <= kCorrected; ++k) {
+        STEP(DOMINO_PHASE_FC1, launch_fc1(c, r, k));
+        STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
+        if (k < kCorrected) STEP(DOMINO_PHASE_GRU, launch_gru(c, r, k + 1));
+    }
+    STEP(DOMINO_PHASE_OTHER, launch_finalize(c, r));
+    if (r.dbg.logits)
+        STEP(DOMINO_PHASE_OTHER, cudaMemcpyAsync(r.dbg.logits, c->L, (size_t)B * kBlock * c->cfg.V * sizeof(float),
+                                                 cudaMemcpyDeviceToDevice, r.st));
+    if (r.dbg.pool && r.K > 0)
+        STEP(DOMINO_PHASE_OTHER, cudaMemcpyAsync(r.dbg.pool, c->pool, (size_t)B * r.K * sizeof(int32_t),
+                                                 cudaMemcpyDeviceToDevice, r.st));
+#undef STEP
+    c->last_launches = r.launches;
+    return DOMINO_OK;
+fail:
+    c->last_launches = r.launches;
+    return DOMINO_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) {
+    if (!out) return DOMINO_ERR_INVALID_ARG;
+    *out = nullptr;
+    int st = check_config(cfg);
+    if (st != DOMINO_OK) return st;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return DOMINO_ERR_CUDA;
+    DeviceGuard guard(device);
+
+    domino_ctx* c = (domino_ctx*)calloc(1, sizeof(domino_ctx));
+    if (!c) return DOMINO_ERR_OOM;
+    c->cfg = *cfg;
+    c->device = device;
+    if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        free(c);
+        return DOMINO_ERR_CUDA;
+    }
+    const domino_config& g = c->cfg;
+    c->a_rows = (int)align_up((size_t)(g.max_B > 16 ? g.max_B : 16), 16);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    size_t oL = take((size_t)g.max_B * kBlock * g.V * sizeof(float));
+    size_t oS = take(g.max_K > 0 ? (size_t)g.max_B * g.V * sizeof(float) : 0);
+    size_t oP = take((size_t)g.max_B * (g.max_K > 0 ? g.max_K : 1) * sizeof(int32_t));
+    size_t oH = take((size_t)2 * g.max_B * g.G * sizeof(float));
+    size_t oA = take((size_t)g.max_B * g.F * sizeof(float));
+    size_t oA16 = take((size_t)c->a_rows * g.F * sizeof(__nv_bfloat16));
+    size_t oK = take((size_t)g.max_B * kBlock * sizeof(unsigned long long));
+    size_t oBad = take((size_t)g.max_B * sizeof(int));
+    size_t oErr = take(sizeof(int));
+    size_t oSync = take(1024);
+    c->ws_bytes = off;
+    if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free(c);
+        return DOMINO_ERR_OOM;
+    }
+    char* base = (char*)c->ws_base;
+    c->L = (float*)(base + oL);
+    c->score = (float*)(base + oS);
+    c->pool = (int32_t*)(base + oP);
+    c->h = (float*)(base + oH);
+    c->a = (float*)(base + oA);
+    c->a16 = (__nv_bfloat16*)(base + oA16);
+    c->keys = (unsigned long long*)(base + oK);
+    c->bad = (int*)(base + oBad);
+    c->err = (int*)(base + oErr);
+    c->sync = (unsigned int*)(base + oSync);
+    // zero the small state (a16 padding rows must stay zero for the MMA path)
+    if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(c->ws_base);
+        free(c);
+        return DOMINO_ERR_CUDA;
+    }
+    c->driver = DOMINO_DRIVER_AUTO;
+    *out = c;
+    return DOMINO_OK;
+}
+
+int domino_rollout_load_weights(domino_ctx* c, const void* lm_head, const void* emb, const void* w_ih,
+                                const void* w_hh, const void* fc1, const void* fc2, const void* bias) {
+    if (!c || !lm_head || !emb || !w_ih || !w_hh || !fc1 || !fc2 || !bias) return DOMINO_ERR_INVALID_ARG;
+    const void* ps[] = {lm_head, emb, w_ih, w_hh, fc1, fc2, bias};
+    for (const void* p : ps)
+        if (!aligned16(p)) return DOMINO_ERR_INVALID_ARG;
+    c->lm_head = lm_head;
+    c->emb = emb;
+    c->w_ih = w_ih;
+    c->w_hh = w_hh;
+    c->fc1 = fc1;
+    c->fc2 = fc2;
+    c->bias = bias;
+    c->has_tma = false;
+    c->loaded = true;
+    return DOMINO_OK;
+}
+
+int domino_rollout_run(domino_ctx* c, const void* hidden, const void* s, const int32_t* verified, int B, int K,
+                       int32_t* out_tokens, void* stream) {
+    return run_impl(c, hidden, s, verified, B, K, nullptr, nullptr, out_tokens, stream);
+}
+
+int domino_rollout_debug_run(domino_ctx* c, const void* hidden, const void* s, const int32_t* verified, int B, int K,
+                             const int32_t* forced, const domino_debug_bufs* dbg, int32_t* out_tokens, void* stream) {
+    return run_impl(c, hidden, s, verified, B, K, forced, dbg, out_tokens, stream);
+}
+
+int domino_rollout_set_driver(domino_ctx* c, int driver) {
+    if (!c) return DOMINO_ERR_INVALID_ARG;
+    if (driver != DOMINO_DRIVER_AUTO && driver != DOMINO_DRIVER_KERNELS && driver != DOMINO_DRIVER_PERSISTENT)
+        return DOMINO_ERR_INVALID_ARG;
+    c->driver = driver;
+    return DOMINO_OK;
+}
+
+int domino_rollout_enable_timing(domino_ctx* c, int enable) {
+    if (!c) return DOMINO_ERR_INVALID_ARG;
+    c->timing = enable != 0;
+    return DOMINO_OK;
+}
+
+int domino_rollout_read_timing(domino_ctx* c, float* ms, int* launches) {
+    if (!c || !ms || !launches) return DOMINO_ERR_INVALID_ARG;
+    DeviceGuard guard(c->device);
+    for (int i = 0; i < c->n_pending; ++i) {
+        float t = 0.f;
+        if (cudaEventSynchronize(c->ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&t, c->ev[2 * i], c->ev[2 * i + 1]) != cudaSuccess) {
+            c->n_pending = 0;
+            return DOMINO_ERR_CUDA;
+        }
+        int p = c->pending_phase[i];
+        if (p >= 0 && p < DOMINO_N_PHASES) {
+            ms[p] += t;
+            launches[p] += 1;
+        }
+    }
+    c->n_pending = 0;
+    return DOMINO_OK;
+}
+
+int domino_rollout_status(domino_ctx* c, void* stream) {
+    if (!c) return DOMINO_ERR_INVALID_ARG;
+    DeviceGuard guard(c->device);
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DOMINO_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, c->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DOMINO_ERR_CUDA;
+    if (word && cudaMemset(c->err, 0, sizeof(int)) != cudaSuccess) return DOMINO_ERR_CUDA;
+    if (word & kErrTimeout) return DOMINO_ERR_TIMEOUT;
+    if (word & kErrBadToken) return DOMINO_ERR_BAD_TOKEN;
+    return DOMINO_OK;
+}
+
+int domino_rollout_last_launch_count(const domino_ctx* c) { return c ? c->last_launches : 0; }
+
+void domino_rollout_destroy(domino_ctx* c) {
+    if (!c) return;
+    {
+        DeviceGuard guard(c->device);
+        cudaDeviceSynchronize();
+        cudaFree(c->ws_base);
+        for (int i = 0; i < c->n_events; ++i) cudaEventDestroy(c->ev[i]);
+    }
+    free(c);
+}
+
+const char* domino_rollout_strerror(int st) {
+    switch (st) {
+        case DOMINO_OK: return "ok";
+        case DOMINO_ERR_INVALID_ARG: return "invalid argument";
+        case DOMINO_ERR_UNSUPPORTED: return "unsupported configuration";
+        case DOMINO_ERR_NOT_LOADED: return "weights not loaded";
+        case DOMINO_ERR_CUDA: return "CUDA error";
+        case DOMINO_ERR_OOM: return "out of device memory";
+        case DOMINO_ERR_TIMEOUT: return "device-side wait timed out";
+        case DOMINO_ERR_BAD_TOKEN: return "token id outside [0, V)";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,168 @@
+// Shared device helpers and the library's internal context.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "domino_rollout.h"
+
+namespace domino {
+
+constexpr int kBlock = DOMINO_BLOCK;       // draft positions per request
+constexpr int kProposals = kBlock - 1;     // p_1 .. p_15
+constexpr int kCorrected = kProposals - 1; // corrected steps k = 1..14
+// Base row used by proposal j (0-based): block position 0 holds the verified
+// token, so proposal j reads row j + 1.
+constexpr int kRowOffset = 1;
+
+// Device error word bits.
+constexpr int kErrBadToken = 1;
+constexpr int kErrTimeout = 2;
+
+// ---------------------------------------------------------------------------
+// argmax keys: (orderable(value) << 32) | ~index.  A larger key is a larger
+// value, and among equal values the lower index.  -0.0 is folded into +0.0 so
+// that signed zeros compare equal, as they do as numbers.
+__device__ __forceinline__ uint32_t ord_f32(float f) {
+    uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord_f32(uint32_t o) {
+    uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    return __uint_as_float(u);
+}
+__device__ __forceinline__ unsigned long long pack_key(float v, uint32_t idx) {
+    return ((unsigned long long)ord_f32(v) << 32) | (unsigned long long)(~idx);
+}
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) {
+    return ~(uint32_t)(k & 0xFFFFFFFFull);
+}
+__device__ __forceinline__ float key_value(unsigned long long k) {
+    return unord_f32((uint32_t)(k >> 32));
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+        k = other > k ? other : k;
+    }
+    return k;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------------------
+// element loads: 8 consecutive elements widened to fp32
+__device__ __forceinline__ void load8(const float* p, float* o) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* o) {
+    uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+    bf16x2_to_f32(q.x, o[0], o[1]);
+    bf16x2_to_f32(q.y, o[2], o[3]);
+    bf16x2_to_f32(q.z, o[4], o[5]);
+    bf16x2_to_f32(q.w, o[6], o[7]);
+}
+// streaming variant: do not keep the line in L1
+__device__ __forceinline__ void load8_stream(const __nv_bfloat16* p, float* o) {
+    uint4 q;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w) : "l"(p));
+    bf16x2_to_f32(q.x, o[0], o[1]);
+    bf16x2_to_f32(q.y, o[2], o[3]);
+    bf16x2_to_f32(q.z, o[4], o[5]);
+    bf16x2_to_f32(q.w, o[6], o[7]);
+}
+__device__ __forceinline__ void load8_stream(const float* p, float* o) { load8(p, o); }
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Warp-cooperative dot product of one weight row (n elements of T) with a
+// fp32 vector; every lane returns the full sum.
+template <typename T>
+__device__ __forceinline__ float warp_dot(const T* __restrict__ w, const float* __restrict__ x, int n, int lane) {
+    float acc = 0.f;
+    if ((n & 7) == 0) {
+        for (int i = lane * 8; i < n; i += 256) {
+            float e[8];
+            load8(w + i, e);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc = fmaf(e[j], x[i + j], acc);
+        }
+    } else {
+        for (int i = lane; i < n; i += 32) acc = fmaf(to_f32(w[i]), x[i], acc);
+    }
+    return warp_sum(acc);
+}
+// Same, with the vector in the weight dtype (e.g. an embedding row).
+template <typename T>
+__device__ __forceinline__ float warp_dot_tt(const T* __restrict__ w, const T* __restrict__ x, int n, int lane) {
+    float acc = 0.f;
+    if ((n & 7) == 0) {
+        for (int i = lane * 8; i < n; i += 256) {
+            float e[8], f[8];
+            load8(w + i, e);
+            load8(x + i, f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc = fmaf(e[j], f[j], acc);
+        }
+    } else {
+        for (int i = lane; i < n; i += 32) acc = fmaf(to_f32(w[i]), to_f32(x[i]), acc);
+    }
+    return warp_sum(acc);
+}
+
+}  // namespace domino
+
+// ---------------------------------------------------------------------------
+// Library context (opaque to callers).
+struct domino_ctx {
+    domino_config cfg;
+    int device;
+    int num_sms;
+    int driver;
+    int last_launches;
+    bool loaded;
+    // borrowed weights
+    const void *lm_head, *emb, *w_ih, *w_hh, *fc1, *fc2, *bias;
+    // workspace (owned)
+    float* L;                 // [max_B,16,V]
+    float* score;             // [max_B,V]
+    int32_t* pool;            // [max_B,max_K]
+    float* h;                 // [2][max_B,G] ping-pong
+    float* a;                 // [max_B,F]
+    __nv_bfloat16* a16;       // [a_rows,F] bf16 copy of a, zero padded
+    int a_rows;
+    unsigned long long* keys; // [max_B,16] argmax words, one per proposal
+    int* bad;                 // [max_B] request saw an invalid token
+    int* err;                 // device error word
+    unsigned int* sync;       // grid-barrier words for the persistent driver
+    void* ws_base;            // single workspace allocation
+    size_t ws_bytes;
+    // TMA descriptors (bf16 path)
+    CUtensorMap tm_lm_head;
+    CUtensorMap tm_fc2;
+    bool has_tma;
+    // per-phase timing (host side)
+    bool timing;
+    int n_pending;
+    int pending_phase[4096];
+    cudaEvent_t ev[2 * 4096];
+    int n_events;  // created so far
+};

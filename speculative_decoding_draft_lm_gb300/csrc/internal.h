@@ -1,0 +1,41 @@
+// Host-side launch interface shared by the library's translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace domino {
+
+struct RunArgs {
+    const void* hidden;        // [B,16,H]
+    const void* s;             // [B,15,F]
+    const int32_t* verified;   // [B]
+    int B;
+    int K;                     // effective pool size: 0 = full vocabulary
+    const int32_t* forced;     // nullable [B,15]
+    domino_debug_bufs dbg;     // all-null when not debugging
+    int32_t* out_tokens;       // [B,15]
+    cudaStream_t st;
+    int launches;              // incremented per kernel launch
+};
+
+// SIMT kernels (kernels_simt.cu)
+cudaError_t launch_reset(domino_ctx* c, RunArgs& r);
+cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r);
+cudaError_t launch_first_argmax(domino_ctx* c, RunArgs& r);
+cudaError_t launch_pool_select(domino_ctx* c, RunArgs& r, bool score_ready);
+// GRU update u (0..14): u = 0 consumes the verified token with h = 0,
+// u >= 1 consumes proposal u-1 (or forced[:,u-1]).
+cudaError_t launch_gru(domino_ctx* c, RunArgs& r, int u);
+cudaError_t launch_fc1(domino_ctx* c, RunArgs& r, int k);
+cudaError_t launch_correct_simt(domino_ctx* c, RunArgs& r, int k);
+cudaError_t launch_finalize(domino_ctx* c, RunArgs& r);
+cudaError_t prepare_simt_kernels(domino_ctx* c);
+
+// tcgen05 / TMA kernels (lmhead_tc.cu)
+bool lmhead_tc_supported(const domino_ctx* c);
+cudaError_t launch_lmhead_tc(domino_ctx* c, RunArgs& r);
+
+// index of the ping-pong h buffer written by GRU update u
+inline int h_slot(int u) { return u & 1; }
+
+}  // namespace domino
