@@ -93,12 +93,16 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         if (e != cudaSuccess) goto fail;                 \
     } while (0)
     STEP(DOMINO_PHASE_OTHER, launch_reset(c, r));
-    if (c->cfg.dtype == DOMINO_DTYPE_BF16 && lmhead_tc_supported(c))
-        STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_tc(c, r));
-    else
-        STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_simt(c, r));
-    STEP(DOMINO_PHASE_ARGMAX, launch_first_argmax(c, r));
-    if (r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, false));
+    {
+        const bool tc_path = lmhead_tc_supported(c);
+        if (tc_path) {
+            STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_tc(c, r));
+        } else {
+            STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_simt(c, r));
+            STEP(DOMINO_PHASE_ARGMAX, launch_first_argmax(c, r));
+        }
+        if (r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, tc_path));
+    }
     STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 0));
     STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 1));
     for (int k = 1; k <= kCorrected; ++k) {
@@ -203,6 +207,16 @@ int domino_rollout_load_weights(domino_ctx* c, const void* lm_head, const void* 
     c->fc2 = fc2;
     c->bias = bias;
     c->has_tma = false;
+    if (c->cfg.dtype == DOMINO_DTYPE_BF16) {
+        DeviceGuard guard(c->device);
+        const domino_config& g = c->cfg;
+        if (make_tmap_bf16(&c->tm_lm_head, lm_head, (uint64_t)g.V, (uint64_t)g.H, 128) != cudaSuccess ||
+            make_tmap_bf16(&c->tm_fc2, fc2, (uint64_t)g.V, (uint64_t)g.F, 128) != cudaSuccess) {
+            c->loaded = false;
+            return DOMINO_ERR_CUDA;
+        }
+        c->has_tma = true;
+    }
     c->loaded = true;
     return DOMINO_OK;
 }

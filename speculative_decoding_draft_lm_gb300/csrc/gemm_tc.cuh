@@ -1,0 +1,204 @@
+// Persistent tcgen05 "skinny" GEMM core: D[128 x BN] tiles of A[M,K] . B[N,K]^T
+// with A streamed from HBM and B (a few activation rows) re-read from L2.
+//
+//   warp 0      TMA producer (one elected thread): A box {64, 128} and B box
+//               {64, BN} per k-chunk into a STAGES-deep ring, 128-byte swizzle
+//   warp 1      TMEM allocator + MMA issuer (one thread): 4 x tcgen05.mma
+//               (M=128, N=BN, K=16) per k-chunk into one of two TMEM
+//               accumulators, tcgen05.commit frees the ring slot
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               row of A), handed to the Epi functor 16 columns at a time
+//
+// Tiles are visited m-major (tile t -> m = t / n_tiles, n = t % n_tiles), grid
+// stride over a persistent grid of one CTA per SM, so CTAs that share an A
+// tile run at the same time.  Every wait is bounded (tc::mbar_wait); on a
+// timeout the block drains its copies and MMAs, frees TMEM and returns with
+// the device error word set.
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace domino {
+namespace tc {
+
+constexpr int kBM = 128;          // rows of A per tile (MMA M)
+constexpr int kBK = 64;           // K elements per chunk (128 bytes of bf16)
+constexpr int kGemmThreads = 192;
+
+template <int BN>
+struct GemmShape {
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (196608 / STAGE) > 12 ? 12 : (196608 / STAGE);
+    static constexpr int TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 512;
+};
+
+template <int BN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+              int K, Epi epi, int* err) {
+    using S = GemmShape<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S::STAGES * S::STAGE);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* consumed_ptr = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S::STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * S::STAGES), tempty0 = tfull0 + 16, drain = tfull0 + 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *consumed_ptr = 0;
+        fence_barrier_init();
+        fence_proxy_async();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int m_tiles = (M + kBM - 1) / kBM;
+    const int n_tiles = (N + BN - 1) / BN;
+    const int k_iters = (K + kBK - 1) / kBK;
+    const int tiles = m_tiles * n_tiles;
+    int issued = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol_a = policy_evict_first();
+            const uint64_t pol_b = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+                const int m = t / n_tiles, n = t % n_tiles;
+                for (int kk = 0; kk < k_iters; ++kk) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) break;
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * S::STAGE);
+                    mbar_arrive_expect_tx(full0 + 8 * stage, S::STAGE);
+                    tma_load_2d(sa, &tmA, kk * kBK, m * kBM, full0 + 8 * stage, pol_a);
+                    tma_load_2d(sa + S::A_BYTES, &tmB, kk * kBK, n * BN, full0 + 8 * stage, pol_b);
+                    ++issued;
+                    if (++stage == S::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int consumed = 0;
+            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int kk = 0; kk < k_iters; ++kk) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * S::STAGE);
+                    const uint32_t sb = sa + S::A_BYTES;
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j)
+                        mma_bf16(d, sdesc_sw128(sa + 32 * j), sdesc_sw128(sb + 32 * j), idesc, (kk | j) != 0);
+                    mma_commit(empty0 + 8 * stage);
+                    *consumed_ptr = ++consumed;
+                    if (++stage == S::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull0 + 8 * acc);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            // all MMAs issued by this thread are complete once `drain` fires
+            mma_commit(drain);
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(drain, 0)) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    atomicOr(err, kErrTimeout);
+                    break;
+                }
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) break;
+            tc_fence_after();
+            const int m = t / n_tiles, n = t % n_tiles;
+            const int row = m * kBM + quarter * 32 + lane;
+            const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 16; ++c) {
+                float v[16];
+                tmem_ld16(tbase + 16 * c, v);
+                epi(n * BN + 16 * c, row, v, lane);
+            }
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag && warp == 0 && lane == 0) {
+        // let every copy this block issued land before the block exits
+        const int consumed = *consumed_ptr;
+        for (int i = consumed; i < issued; ++i) {
+            const int s = i % S::STAGES;
+            const uint32_t par = (uint32_t)((i / S::STAGES) & 1);
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(full0 + 8 * s, par) && globaltimer() - t0 < 2000000ull) {
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, S::TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+}  // namespace domino

@@ -32,7 +32,9 @@ cudaError_t launch_finalize(domino_ctx* c, RunArgs& r);
 cudaError_t prepare_simt_kernels(domino_ctx* c);
 
 // tcgen05 / TMA kernels (lmhead_tc.cu)
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 bool lmhead_tc_supported(const domino_ctx* c);
+// also writes p_1's argmax word and, when r.K > 0, the pool scores
 cudaError_t launch_lmhead_tc(domino_ctx* c, RunArgs& r);
 
 // index of the ping-pong h buffer written by GRU update u

@@ -1,7 +1,121 @@
-// Tensor-core LM-head (tcgen05 + TMA); placeholder until the kernel lands.
+// Base LM-head on the tensor cores (bf16 in, fp32 accumulate):
+//   L[b, i, v] = sum_h hidden[b, i, h] * lm_head[v, h]   for all 16 block rows,
+// with the first-proposal argmax (row 1) and, in pool mode, the per-request
+// pool score max_{i=1..15} L[b, i, v] fused into the epilogue, so the logits
+// are written to HBM once and never re-read for those two reductions.
+//
+// Method: page "support tensor-parallel Domino rollout", section "Rollout
+// performance" (step-major base LM-head) and page "Add correctness-first
+// Domino support to DFlash V2", section "Design" (full-vocabulary base
+// projection, first proposal = its argmax, block-shared pool).
+//
+// Orientation: vocabulary rows are the MMA's M (128 per tile, A = lm_head,
+// streamed once), the B*16 draft rows are N (B operand, L2-resident).
+#include "gemm_tc.cuh"
 #include "internal.h"
 
+#include <cudaTypedefs.h>
+
 namespace domino {
-bool lmhead_tc_supported(const domino_ctx*) { return false; }
-cudaError_t launch_lmhead_tc(domino_ctx*, RunArgs&) { return cudaErrorNotSupported; }
+
+namespace {
+
+struct EpiLmHead {
+    float* L;                  // [B,16,V]
+    unsigned long long* keys;  // [B,16], slot 0 = p_1
+    float* score;              // [B,V] or null
+    int V, B;
+    __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane) const {
+        const int b = col0 >> 4;  // 16 columns = the 16 block rows of request b
+        if (b >= B) return;       // uniform across the warp
+        const bool ok = row < V;
+        if (ok) {
+            float* dst = L + (size_t)b * kBlock * V + row;
+#pragma unroll
+            for (int i = 0; i < kBlock; ++i) dst[(size_t)i * V] = v[i];
+            if (score) {
+                float m = v[kRowOffset];
+#pragma unroll
+                for (int i = kRowOffset + 1; i < kRowOffset + kProposals; ++i) m = fmaxf(m, v[i]);
+                score[(size_t)b * V + row] = m;
+            }
+        }
+        unsigned long long key = ok ? pack_key(v[kRowOffset], (uint32_t)row) : 0ull;
+        key = warp_max_u64(key);
+        if (lane == 0 && key) atomicMax(&keys[(size_t)b * kBlock], key);
+    }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <int BN>
+cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, float* score) {
+    using S = tc::GemmShape<BN>;
+    static bool attr_set[64] = {};
+    auto kern = tc::k_gemm_tc<BN, EpiLmHead>;
+    const int slot = c->device & 63;
+    if (!attr_set[slot]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[slot] = true;
+    }
+    const int N = r.B * kBlock;
+    const int tiles = ((c->cfg.V + tc::kBM - 1) / tc::kBM) * ((N + BN - 1) / BN);
+    const int grid = tiles < c->num_sms ? tiles : c->num_sms;
+    EpiLmHead epi{c->L, c->keys, score, c->cfg.V, r.B};
+    kern<<<grid, tc::kGemmThreads, S::SMEM, r.st>>>(c->tm_lm_head, tmB, c->cfg.V, N, c->cfg.H, epi, c->err);
+    ++r.launches;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box {64, box_rows},
+// 128-byte swizzle, zero fill outside the matrix.
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)tc::kBK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+bool lmhead_tc_supported(const domino_ctx* c) { return c->has_tma && c->cfg.dtype == DOMINO_DTYPE_BF16; }
+
+int lmhead_bn(int B) {
+    const int N = B * kBlock;
+    return N <= 16 ? 16 : N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+}
+
+cudaError_t launch_lmhead_tc(domino_ctx* c, RunArgs& r) {
+    const int BN = lmhead_bn(r.B);
+    CUtensorMap tmB;
+    cudaError_t e = make_tmap_bf16(&tmB, r.hidden, (uint64_t)r.B * kBlock, (uint64_t)c->cfg.H, (uint32_t)BN);
+    if (e != cudaSuccess) return e;
+    float* score = r.K > 0 ? c->score : nullptr;
+    switch (BN) {
+        case 16: return launch_bn<16>(c, r, tmB, score);
+        case 32: return launch_bn<32>(c, r, tmB, score);
+        case 64: return launch_bn<64>(c, r, tmB, score);
+        case 128: return launch_bn<128>(c, r, tmB, score);
+        default: return launch_bn<256>(c, r, tmB, score);
+    }
+}
+
 }  // namespace domino
