@@ -83,6 +83,14 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     r.out_tokens = out;
     r.st = (cudaStream_t)stream;
 
+    bool use_persist = false;
+    if (c->driver == DOMINO_DRIVER_PERSISTENT) {
+        if (!persist_supported(c, r)) return DOMINO_ERR_UNSUPPORTED;
+        use_persist = true;
+    } else if (c->driver == DOMINO_DRIVER_AUTO) {
+        use_persist = persist_supported(c, r);
+    }
+
     cudaError_t e;
 #define STEP(phase, x)                                   \
     do {                                                 \
@@ -103,12 +111,29 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         }
         if (r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, tc_path));
     }
+    if (use_persist) {
+        STEP(DOMINO_PHASE_STEPS, launch_persist(c, r));
+    } else {
     STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 0));
     STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 1));
-    for (int k = 1; k <= kCorrected; ++k) {
-        STEP(DOMINO_PHASE_FC1, launch_fc1(c, r, k));
-        STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
-        if (k < kCorrected) STEP(DOMINO_PHASE_GRU, launch_gru(c, r, k + 1));
+    {
+        // tensor cores once the full-vocabulary correction is a real
+        // contraction (two or more requests); CUDA cores for B = 1 and pools
+        const bool tc_corr = r.B >= 2 && correct_tc_supported(c, r);
+        CUtensorMap tm_a;
+        if (tc_corr) {
+            e = prepare_correct_tc(c, r, &tm_a);
+            if (e != cudaSuccess) goto fail;
+        }
+        for (int k = 1; k <= kCorrected; ++k) {
+            STEP(DOMINO_PHASE_FC1, launch_fc1(c, r, k));
+            if (tc_corr)
+                STEP(DOMINO_PHASE_CORRECT, launch_correct_tc(c, r, tm_a, k));
+            else
+                STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
+            if (k < kCorrected) STEP(DOMINO_PHASE_GRU, launch_gru(c, r, k + 1));
+        }
+    }
     }
     STEP(DOMINO_PHASE_OTHER, launch_finalize(c, r));
     if (r.dbg.logits)

@@ -1,0 +1,99 @@
+// Correction + argmax of one corrected step over the full vocabulary on the
+// tensor cores, for batches of independent requests:
+//   c[b, v] = fc2[v, :] . a[b, :] + bias[v] + L[b, k+1, v],
+//   p_{k+1}[b] = argmax_v c[b, v]   (lowest id on ties).
+// fc2 is streamed once per step as the MMA's A operand (128 vocabulary rows
+// per tile); the bf16 activations a[b, :] of all requests form the N side.
+//
+// Method: page "[Spec] Add Domino projector support to DFlash speculative
+// decoding (V2)", section "Implementation" (fused SiLU(z+s) @ fc2^T + bias +
+// base_logits full-vocabulary argmax) and page "Add correctness-first Domino
+// support to DFlash V2", section "Design" (full-vocabulary correction, K=0).
+// The activations are rounded to bf16 for the MMA; accumulation is fp32.
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace domino {
+
+namespace {
+
+struct EpiCorrect {
+    const __nv_bfloat16* bias;  // [V]
+    const float* L;             // [B,16,V]
+    unsigned long long* keys;   // [B,16]
+    float* dbg_scores;          // [B,14,V] or null
+    int V, B, k;
+    __device__ __forceinline__ void begin(unsigned long long* sb, int t) const {
+        for (int i = t; i < tc::kEpiScratch; i += 128) sb[i] = 0ull;
+    }
+    __device__ __forceinline__ void end(unsigned long long* sb, int t) const {
+        const int n = B < tc::kEpiScratch ? B : tc::kEpiScratch;
+        for (int b = t; b < n; b += 128)
+            if (sb[b]) atomicMax(&keys[(size_t)b * kBlock + k], sb[b]);
+    }
+    __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane,
+                                               unsigned long long* sb) const {
+        if (col0 >= B) return;  // uniform: padding columns
+        const bool ok = row < V;
+        const float bv = ok ? __bfloat162float(bias[row]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int b = col0 + j;
+            if (b >= B) break;  // uniform
+            float c = 0.f;
+            if (ok) {
+                c = v[j] + bv + L[((size_t)b * kBlock + kRowOffset + k) * V + row];
+                if (dbg_scores) dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + row] = c;
+            }
+            unsigned long long key = ok ? pack_key(c, (uint32_t)row) : 0ull;
+            key = warp_max_u64(key);
+            if (lane == 0 && key) {
+                if (b < tc::kEpiScratch) atomicMax(&sb[b], key);
+                else atomicMax(&keys[(size_t)b * kBlock + k], key);
+            }
+        }
+    }
+};
+
+template <int BN>
+cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) {
+    using S = tc::GemmShape<BN>;
+    static bool attr_set[64] = {};
+    auto kern = tc::k_gemm_tc<BN, EpiCorrect>;
+    const int slot = c->device & 63;
+    if (!attr_set[slot]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[slot] = true;
+    }
+    const int tiles = ((c->cfg.V + tc::kBM - 1) / tc::kBM) * ((r.B + BN - 1) / BN);
+    const int grid = tiles < c->num_sms ? tiles : c->num_sms;
+    EpiCorrect epi{(const __nv_bfloat16*)c->bias, c->L, c->keys, r.dbg.scores, c->cfg.V, r.B, k};
+    kern<<<grid, tc::kGemmThreads, S::SMEM, r.st>>>(c->tm_fc2, tmB, c->cfg.V, r.B, c->cfg.F, epi, c->err);
+    ++r.launches;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int correct_bn(int B) { return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : B <= 128 ? 128 : 256; }
+
+bool correct_tc_supported(const domino_ctx* c, const RunArgs& r) {
+    return c->has_tma && c->cfg.dtype == DOMINO_DTYPE_BF16 && r.K == 0 && r.B <= c->a_rows;
+}
+
+cudaError_t prepare_correct_tc(domino_ctx* c, RunArgs& r, CUtensorMap* tmB) {
+    return make_tmap_bf16(tmB, c->a16, (uint64_t)c->a_rows, (uint64_t)c->cfg.F, (uint32_t)correct_bn(r.B));
+}
+
+cudaError_t launch_correct_tc(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) {
+    switch (correct_bn(r.B)) {
+        case 16: return launch_bn<16>(c, r, tmB, k);
+        case 32: return launch_bn<32>(c, r, tmB, k);
+        case 64: return launch_bn<64>(c, r, tmB, k);
+        case 128: return launch_bn<128>(c, r, tmB, k);
+        default: return launch_bn<256>(c, r, tmB, k);
+    }
+}
+
+}  // namespace domino

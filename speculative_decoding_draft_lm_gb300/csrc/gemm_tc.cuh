@@ -9,6 +9,10 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
 //               row of A), handed to the Epi functor 16 columns at a time
 //
+// Epi provides begin(scratch, t) / operator()(col0, row, v[16], lane, scratch)
+// / end(scratch, t), t = epilogue thread 0..127; `scratch` is kEpiScratch
+// per-block 64-bit words (per-request argmax words) in shared memory.
+//
 // Tiles are visited m-major (tile t -> m = t / n_tiles, n = t % n_tiles), grid
 // stride over a persistent grid of one CTA per SM, so CTAs that share an A
 // tile run at the same time.  Every wait is bounded (tc::mbar_wait); on a
@@ -24,6 +28,9 @@ namespace tc {
 constexpr int kBM = 128;          // rows of A per tile (MMA M)
 constexpr int kBK = 64;           // K elements per chunk (128 bytes of bf16)
 constexpr int kGemmThreads = 192;
+constexpr int kEpiScratch = 256;  // 64-bit words
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int BN>
 struct GemmShape {
@@ -32,7 +39,7 @@ struct GemmShape {
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = (196608 / STAGE) > 12 ? 12 : (196608 / STAGE);
     static constexpr int TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 512;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 512 + 8 * kEpiScratch;
 };
 
 template <int BN, class Epi>
@@ -47,6 +54,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* consumed_ptr = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    unsigned long long* scratch = reinterpret_cast<unsigned long long*>(smem + (size_t)S::STAGES * S::STAGE + 512);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S::STAGES);
@@ -159,8 +167,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         const int quarter = warp & 3;
+        const int et = threadIdx.x - 64;
         int acc = 0;
         uint32_t acc_phase = 0;
+        epi.begin(scratch, et);
+        epi_bar();
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) break;
             tc_fence_after();
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int c = 0; c < BN / 16; ++c) {
                 float v[16];
                 tmem_ld16(tbase + 16 * c, v);
-                epi(n * BN + 16 * c, row, v, lane);
+                epi(n * BN + 16 * c, row, v, lane, scratch);
             }
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
@@ -180,6 +191,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 acc_phase ^= 1;
             }
         }
+        epi_bar();
+        epi.end(scratch, et);
     }
     __syncthreads();
     if (*abort_flag && warp == 0 && lane == 0) {

@@ -37,7 +37,16 @@ bool lmhead_tc_supported(const domino_ctx* c);
 // also writes p_1's argmax word and, when r.K > 0, the pool scores
 cudaError_t launch_lmhead_tc(domino_ctx* c, RunArgs& r);
 
+// tcgen05 correction over the full vocabulary (correct_tc.cu)
+bool correct_tc_supported(const domino_ctx* c, const RunArgs& r);
+cudaError_t prepare_correct_tc(domino_ctx* c, RunArgs& r, CUtensorMap* tmB);
+cudaError_t launch_correct_tc(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k);
+
+// persistent driver of the GRU seed and the 14 corrected steps (persist.cu)
+bool persist_supported(const domino_ctx* c, const RunArgs& r);
+cudaError_t launch_persist(domino_ctx* c, RunArgs& r);
+
 // index of the ping-pong h buffer written by GRU update u
-inline int h_slot(int u) { return u & 1; }
+__host__ __device__ inline int h_slot(int u) { return u & 1; }
 
 }  // namespace domino

@@ -19,10 +19,12 @@ inline int grid_for(int items_per_block_unit, int units, int cap) {
 }
 
 // ---------------------------------------------------------------------------
-__global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__ bad, int n_keys, int B) {
+__global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__ bad, unsigned* __restrict__ sync,
+                        int n_keys, int B) {
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n_keys) keys[i] = 0ull;
     if (i < B) bad[i] = 0;
+    if (i < 4) sync[i] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -398,7 +400,7 @@ __global__ void k_finalize(const unsigned long long* __restrict__ keys, const in
 
 cudaError_t launch_reset(domino_ctx* c, RunArgs& r) {
     int n = r.B * kBlock;
-    k_reset<<<(n + 255) / 256, 256, 0, r.st>>>(c->keys, c->bad, n, r.B);
+    k_reset<<<(n + 255) / 256, 256, 0, r.st>>>(c->keys, c->bad, c->sync, n, r.B);
     DOMINO_LAUNCH_CHECK();
     return cudaSuccess;
 }

@@ -25,7 +25,16 @@ struct EpiLmHead {
     unsigned long long* keys;  // [B,16], slot 0 = p_1
     float* score;              // [B,V] or null
     int V, B;
-    __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane) const {
+    __device__ __forceinline__ void begin(unsigned long long* sb, int t) const {
+        for (int i = t; i < tc::kEpiScratch; i += 128) sb[i] = 0ull;
+    }
+    __device__ __forceinline__ void end(unsigned long long* sb, int t) const {
+        const int n = B < tc::kEpiScratch ? B : tc::kEpiScratch;
+        for (int b = t; b < n; b += 128)
+            if (sb[b]) atomicMax(&keys[(size_t)b * kBlock], sb[b]);
+    }
+    __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane,
+                                               unsigned long long* sb) const {
         const int b = col0 >> 4;  // 16 columns = the 16 block rows of request b
         if (b >= B) return;       // uniform across the warp
         const bool ok = row < V;
@@ -42,7 +51,10 @@ struct EpiLmHead {
         }
         unsigned long long key = ok ? pack_key(v[kRowOffset], (uint32_t)row) : 0ull;
         key = warp_max_u64(key);
-        if (lane == 0 && key) atomicMax(&keys[(size_t)b * kBlock], key);
+        if (lane == 0 && key) {
+            if (b < tc::kEpiScratch) atomicMax(&sb[b], key);
+            else atomicMax(&keys[(size_t)b * kBlock], key);
+        }
     }
 };
 

@@ -1,0 +1,585 @@
+// Persistent single-launch driver of the rollout after the LM-head: the two
+// GRU seed updates and the 14 dependent corrected steps run in one
+// cooperative kernel (one CTA per SM) separated by software grid barriers.
+//
+// Per corrected step k (page "Add correctness-first Domino support to DFlash
+// V2", section "Design"; page "[Spec] Add Domino projector support to DFlash
+// speculative decoding (V2)", section "Implementation"):
+//   phase B  a = SiLU(fc1 h + s[k])        each CTA: a slice of the F outputs
+//   -- grid barrier --
+//   phase C  c[v] = fc2[v].a + bias[v] + L[b,k+1,v], argmax   each CTA: a
+//            contiguous slice of fc2 rows (full vocabulary) or of the pool
+//            entries; per-CTA best folded into the step's argmax word
+//   -- grid barrier --
+//   phase A  h = GRU(emb[p_{k+1}], h)      each CTA: a slice of the G outputs
+//   -- grid barrier --
+//
+// A producer warp streams the fc2 rows (contiguous slices, or one row per
+// pool entry) with cp.async.bulk into a ring of shared-memory slots.  The rows
+// are the same at every step, so the producer runs ahead across phases and
+// steps: while the CTA computes the GRU and fc1 phases and waits at barriers
+// the ring refills.  Successive steps walk the slice in opposite directions,
+// so a step starts on the rows the previous one read last (still in L2).
+//
+// The correction here runs on CUDA cores (one warp per row, fp32 FMA), which
+// suits one request per row: B = 1 over the full vocabulary, or pool entries
+// of any request.  Every wait (grid barrier, ring slot) is bounded; on a
+// timeout the kernel raises the device error word and returns.
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace domino {
+
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kPersistThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRowsPerSlot = 16;   // one row per consumer warp per slot
+constexpr int kMaxReq = 8;         // requests a CTA may touch in phase C
+constexpr int kGruGroup = 4;       // requests per GRU/fc1 staging group
+constexpr int kMaxSeg = 2048;      // rows (or pool entries) per CTA
+
+template <typename T>
+struct PersistParams {
+    const T *emb, *w_ih, *w_hh, *fc1, *fc2, *bias, *s;
+    const int32_t *verified, *forced, *pool;
+    const float* L;
+    float* h;       // [2][max_B*G]
+    float* a;       // [max_B*F]
+    unsigned long long* keys;
+    int *bad, *err;
+    unsigned int* sync;
+    float *dbg_h, *dbg_z, *dbg_scores;
+    int B, K, V, E, G, F, max_B;
+    int seg;        // rows (K0) or pool entries per CTA
+    int n_slots;
+    int slot_bytes;
+};
+
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier among the consumer warps of every CTA.  `n` counts barriers
+// passed so far; the counter was zeroed before the launch.
+__device__ bool grid_sync(unsigned* counter, unsigned& n, volatile int* abort_flag, int* err) {
+    cons_sync();
+    ++n;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1u);
+        const unsigned target = n * gridDim.x;
+        const unsigned long long t0 = tc::globaltimer();
+        while (ld_acquire(counter) < target) {
+            if (*abort_flag) break;
+            if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(err, kErrTimeout);
+                break;
+            }
+        }
+        __threadfence();
+    }
+    cons_sync();
+    return !*abort_flag;
+}
+
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// 8 consecutive elements of a shared-memory row widened to fp32
+__device__ __forceinline__ void lds8(const float* p, float* o) {
+    float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+}
+__device__ __forceinline__ void lds8(const __nv_bfloat16* p, float* o) {
+    uint4 q = *reinterpret_cast<const uint4*>(p);
+    bf16x2_to_f32(q.x, o[0], o[1]);
+    bf16x2_to_f32(q.y, o[2], o[3]);
+    bf16x2_to_f32(q.z, o[4], o[5]);
+    bf16x2_to_f32(q.w, o[6], o[7]);
+}
+
+// Shared-memory layout (bytes, all offsets 128-aligned)
+struct Layout {
+    int ring, bars, sa, sx, sh, sg, sL, sbias, sbest, stok, misc, total;
+    __host__ __device__ Layout(int n_slots, int slot_bytes, int E, int G, int F, int seg, int B) {
+        auto up = [](int x) { return (x + 127) & ~127; };
+        const int nreq = B < kMaxReq ? B : kMaxReq, ngru = B < kGruGroup ? B : kGruGroup;
+        int o = 0;
+        ring = o; o = up(o + n_slots * slot_bytes);
+        bars = o; o = up(o + 16 * n_slots);
+        sa = o;   o = up(o + 4 * nreq * F);
+        sx = o;   o = up(o + 4 * ngru * E);
+        sh = o;   o = up(o + 4 * ngru * G);
+        sg = o;   o = up(o + 4 * 6 * kGruGroup * 64);   // gate pre-activations of <= 64 outputs
+        sL = o;   o = up(o + 4 * seg * nreq);
+        sbias = o; o = up(o + 4 * seg);
+        sbest = o; o = up(o + 8 * kMaxReq);
+        stok = o; o = up(o + 4 * 256);
+        misc = o; o = up(o + 64);
+        total = o;
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistParams<T> p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const Layout lay(p.n_slots, p.slot_bytes, p.E, p.G, p.F, p.seg, p.B);
+    uint8_t* ring = sm + lay.ring;
+    const uint32_t full0 = tc::smem_u32(sm + lay.bars), empty0 = full0 + 8 * p.n_slots;
+    float* sa = reinterpret_cast<float*>(sm + lay.sa);
+    float* sx = reinterpret_cast<float*>(sm + lay.sx);
+    float* sh = reinterpret_cast<float*>(sm + lay.sh);
+    float* sg = reinterpret_cast<float*>(sm + lay.sg);
+    float* sL = reinterpret_cast<float*>(sm + lay.sL);
+    float* sbias = reinterpret_cast<float*>(sm + lay.sbias);
+    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(sm + lay.sbest);
+    int* stok = reinterpret_cast<int*>(sm + lay.stok);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + lay.misc);
+    volatile int* consumed_ptr = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const bool full_vocab = p.K == 0;
+    const int B = p.B, V = p.V, E = p.E, G = p.G, F = p.F;
+    const size_t row_bytes = (size_t)F * sizeof(T);
+
+    // this CTA's slice of correction work: rows [w0, w1) of fc2 (full
+    // vocabulary) or entries [w0, w1) of the flattened [B, K] pool
+    const long long work = full_vocab ? (long long)V : (long long)B * p.K;
+    const long long w0 = min(work, (long long)blockIdx.x * p.seg);
+    const long long w1 = min(work, w0 + p.seg);
+    const int nw = (int)(w1 - w0);
+    const int n_chunks = (nw + kRowsPerSlot - 1) / kRowsPerSlot;
+    const int b_first = full_vocab ? 0 : (nw > 0 ? (int)(w0 / p.K) : 0);
+    const int b_count = full_vocab ? B : (nw > 0 ? (int)((w1 - 1) / p.K) - b_first + 1 : 0);
+
+    if (tid == 0) {
+        for (int s = 0; s < p.n_slots; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *consumed_ptr = 0;
+        tc::fence_barrier_init();
+        tc::fence_proxy_async();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            // full vocabulary: normal priority, so that the rows a step reads last
+            // are still in L2 when the next step (walking backwards) starts;
+            // pool rows are re-read every step: keep them
+            const uint64_t pol = full_vocab ? tc::policy_evict_normal() : tc::policy_evict_last();
+            int q = 0;
+            for (int k = 1; k <= kCorrected && !*abort_flag; ++k) {
+                const bool fwd = (k & 1) != 0;
+                for (int ci = 0; ci < n_chunks; ++ci) {
+                    const int c = fwd ? ci : n_chunks - 1 - ci;
+                    const int slot = q % p.n_slots;
+                    const uint32_t par = (uint32_t)((q / p.n_slots) & 1);
+                    if (!tc::mbar_wait(empty0 + 8 * slot, par ^ 1, abort_flag, p.err)) break;
+                    const int r0 = c * kRowsPerSlot;
+                    const int nr = min(kRowsPerSlot, nw - r0);
+                    const uint32_t dst = tc::smem_u32(ring + (size_t)slot * p.slot_bytes);
+                    tc::mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)(nr * row_bytes));
+                    if (full_vocab) {
+                        tc::bulk_load(dst, p.fc2 + (size_t)(w0 + r0) * F, (uint32_t)(nr * row_bytes), full0 + 8 * slot,
+                                      pol);
+                    } else {
+                        for (int r = 0; r < nr; ++r) {
+                            const int v = p.pool[w0 + r0 + r];
+                            tc::bulk_load(dst + (uint32_t)(r * row_bytes), p.fc2 + (size_t)v * F, (uint32_t)row_bytes,
+                                          full0 + 8 * slot, pol);
+                        }
+                    }
+                    ++q;
+                }
+            }
+            // every copy issued must land before the block exits
+            const unsigned long long t0 = tc::globaltimer();
+            while (*consumed_ptr < q && !*abort_flag && tc::globaltimer() - t0 < tc::kWaitLimitNs) {
+            }
+            if (*consumed_ptr < q) {
+                for (int i = *consumed_ptr; i < q; ++i) {
+                    const int s = i % p.n_slots;
+                    const unsigned long long t1 = tc::globaltimer();
+                    while (!tc::mbar_try_wait(full0 + 8 * s, (uint32_t)((i / p.n_slots) & 1)) &&
+                           tc::globaltimer() - t1 < 2000000ull) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    unsigned nsync = 0;
+    unsigned* counter = p.sync;
+    // static per-CTA bias values of the slice
+    for (int i = tid; i < nw; i += kConsumerWarps * 32) {
+        const int v = full_vocab ? (int)(w0 + i) : p.pool[w0 + i];
+        sbias[i] = to_f32(p.bias[v]);
+    }
+    if (tid < kMaxReq) sbest[tid] = 0ull;
+
+    const int jpc = (G + gridDim.x - 1) / gridDim.x;   // GRU outputs per CTA (<= 64)
+    const int j0 = min(G, (int)blockIdx.x * jpc), j1 = min(G, j0 + jpc), jn = j1 - j0;
+    const int fpc = (F + gridDim.x - 1) / gridDim.x;
+    const int f0 = min(F, (int)blockIdx.x * fpc), f1 = min(F, f0 + fpc);
+
+    // ---- one GRU update u for every request; writes h[slot(u)]
+    auto gru = [&](int u) {
+        const float* h_in = p.h + (size_t)h_slot(u + 1) * p.max_B * G;
+        float* h_out = p.h + (size_t)h_slot(u) * p.max_B * G;
+        if (tid < B) {
+            int t;
+            if (u == 0) t = p.verified[tid];
+            else if (p.forced) t = p.forced[(size_t)tid * kProposals + (u - 1)];
+            else t = (int)key_index(__ldcg(&p.keys[(size_t)tid * kBlock + (u - 1)]));
+            if (t < 0 || t >= V) {
+                if (blockIdx.x == 0) {
+                    p.bad[tid] = 1;
+                    atomicOr(p.err, kErrBadToken);
+                }
+                t = 0;
+            }
+            stok[tid] = t;
+        }
+        cons_sync();
+        for (int g0 = 0; g0 < B; g0 += kGruGroup) {
+            const int ng = min(kGruGroup, B - g0);
+            for (int i = tid; i < ng * E; i += kConsumerWarps * 32) {
+                const int b = i / E, e = i % E;
+                sx[b * E + e] = to_f32(p.emb[(size_t)stok[g0 + b] * E + e]);
+            }
+            if (u > 0)
+                for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
+                    const int b = i / G, e = i % G;
+                    sh[b * G + e] = __ldcg(&h_in[(size_t)(g0 + b) * G + e]);
+                }
+            cons_sync();
+            // one warp per (output j, gate): input and hidden dot products
+            for (int it = warp; it < jn * 3; it += kConsumerWarps) {
+                const int jj = it / 3, gate = it % 3;
+                const T* wi = p.w_ih + (size_t)(gate * G + j0 + jj) * E;
+                const T* wh = p.w_hh + (size_t)(gate * G + j0 + jj) * G;
+                float gi[kGruGroup], gh[kGruGroup];
+#pragma unroll
+                for (int b = 0; b < kGruGroup; ++b) gi[b] = gh[b] = 0.f;
+                for (int e = lane * 8; e < E; e += 256) {
+                    float w[8];
+                    load8(wi + e, w);
+#pragma unroll
+                    for (int b = 0; b < kGruGroup; ++b)
+                        if (b < ng) {
+                            float x[8];
+                            lds8(sx + b * E + e, x);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) gi[b] = fmaf(w[q], x[q], gi[b]);
+                        }
+                }
+                if (u > 0)
+                    for (int e = lane * 8; e < G; e += 256) {
+                        float w[8];
+                        load8(wh + e, w);
+#pragma unroll
+                        for (int b = 0; b < kGruGroup; ++b)
+                            if (b < ng) {
+                                float x[8];
+                                lds8(sh + b * G + e, x);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) gh[b] = fmaf(w[q], x[q], gh[b]);
+                            }
+                    }
+#pragma unroll
+                for (int b = 0; b < kGruGroup; ++b) {
+                    if (b < ng) {
+                        const float si = warp_sum(gi[b]), shh = warp_sum(gh[b]);
+                        if (lane == 0) {
+                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 0] = si;
+                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 1] = shh;
+                        }
+                    }
+                }
+            }
+            cons_sync();
+            for (int i = tid; i < jn * ng; i += kConsumerWarps * 32) {
+                const int jj = i / ng, b = i % ng;
+                const float* gr = sg + ((jj * 3 + 0) * kGruGroup + b) * 2;
+                const float* gz = sg + ((jj * 3 + 1) * kGruGroup + b) * 2;
+                const float* gn = sg + ((jj * 3 + 2) * kGruGroup + b) * 2;
+                const float r = sigmoidf_(gr[0] + gr[1]);
+                const float zg = sigmoidf_(gz[0] + gz[1]);
+                const float n = tanhf(gn[0] + r * gn[1]);
+                const float hp = u > 0 ? sh[b * G + j0 + jj] : 0.f;
+                const float hn = (1.f - zg) * n + zg * hp;
+                h_out[(size_t)(g0 + b) * G + j0 + jj] = hn;
+                if (p.dbg_h) p.dbg_h[((size_t)(g0 + b) * kProposals + u) * G + j0 + jj] = hn;
+            }
+            cons_sync();
+        }
+    };
+
+    // ---- projector layer 1 + SiLU for step k; writes a
+    auto fc1 = [&](int k) {
+        const float* hv = p.h + (size_t)h_slot(k) * p.max_B * G;
+        for (int g0 = 0; g0 < B; g0 += kGruGroup) {
+            const int ng = min(kGruGroup, B - g0);
+            for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
+                const int b = i / G, e = i % G;
+                sh[b * G + e] = __ldcg(&hv[(size_t)(g0 + b) * G + e]);
+            }
+            cons_sync();
+            for (int f = f0 + warp; f < f1; f += kConsumerWarps) {
+                const T* w = p.fc1 + (size_t)f * G;
+                float acc[kGruGroup];
+#pragma unroll
+                for (int b = 0; b < kGruGroup; ++b) acc[b] = 0.f;
+                for (int e = lane * 8; e < G; e += 256) {
+                    float ww[8];
+                    load8(w + e, ww);
+#pragma unroll
+                    for (int b = 0; b < kGruGroup; ++b)
+                        if (b < ng) {
+                            float x[8];
+                            lds8(sh + b * G + e, x);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) acc[b] = fmaf(ww[q], x[q], acc[b]);
+                        }
+                }
+#pragma unroll
+                for (int b = 0; b < kGruGroup; ++b) {
+                    if (b < ng) {
+                        float z = warp_sum(acc[b]);
+                        if (lane == 0) {
+                            z += to_f32(p.s[((size_t)(g0 + b) * kProposals + k) * F + f]);
+                            p.a[(size_t)(g0 + b) * F + f] = z * sigmoidf_(z);
+                            if (p.dbg_z) p.dbg_z[((size_t)(g0 + b) * kCorrected + (k - 1)) * F + f] = z;
+                        }
+                    }
+                }
+            }
+            cons_sync();
+        }
+    };
+
+    // ---- correction + argmax of step k over this CTA's slice
+    int q = 0;  // ring position, in step with the producer
+    auto correct = [&](int k) {
+        // activations of the requests this slice touches
+        for (int i = tid; i < b_count * F; i += kConsumerWarps * 32) {
+            const int b = i / F, f = i % F;
+            sa[b * F + f] = __ldcg(&p.a[(size_t)(b_first + b) * F + f]);
+        }
+        cp_async_wait_all();
+        cons_sync();
+        unsigned long long best = 0ull;
+        int cur = -1;
+        const bool fwd = (k & 1) != 0;
+        for (int ci = 0; ci < n_chunks; ++ci) {
+            const int c = fwd ? ci : n_chunks - 1 - ci;
+            const int slot = q % p.n_slots;
+            if (!tc::mbar_wait(full0 + 8 * slot, (uint32_t)((q / p.n_slots) & 1), abort_flag, p.err)) break;
+            const int r = c * kRowsPerSlot + warp;
+            if (r < nw) {
+                const T* wrow = reinterpret_cast<const T*>(ring + (size_t)slot * p.slot_bytes + (size_t)warp * row_bytes);
+                if (full_vocab) {
+                    const int v = (int)(w0 + r);
+                    for (int b = 0; b < B; ++b) {
+                        float acc = 0.f;
+                        for (int f = lane * 8; f < F; f += 256) {
+                            float w[8], x[8];
+                            lds8(wrow + f, w);
+                            lds8(sa + b * F + f, x);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
+                        }
+                        acc = warp_sum(acc);
+                        if (lane == 0) {
+                            const float cv = acc + sbias[r] + sL[b * p.seg + r];
+                            const unsigned long long key = pack_key(cv, (uint32_t)v);
+                            if (B == 1) best = key > best ? key : best;
+                            else atomicMax(&sbest[b], key);
+                            if (p.dbg_scores) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
+                        }
+                    }
+                } else {
+                    const long long item = w0 + r;
+                    const int b = (int)(item / p.K), i = (int)(item % p.K);
+                    const int bl = b - b_first;
+                    float acc = 0.f;
+                    for (int f = lane * 8; f < F; f += 256) {
+                        float w[8], x[8];
+                        lds8(wrow + f, w);
+                        lds8(sa + bl * F + f, x);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
+                    }
+                    acc = warp_sum(acc);
+                    if (lane == 0) {
+                        const float cv = acc + sbias[r] + sL[r];
+                        const unsigned long long key = pack_key(cv, (uint32_t)p.pool[item]);
+                        if (bl != cur) {
+                            if (cur >= 0 && best) atomicMax(&sbest[cur], best);
+                            cur = bl;
+                            best = 0ull;
+                        }
+                        best = key > best ? key : best;
+                        if (p.dbg_scores) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + i] = cv;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
+            ++q;
+            if (tid == 0) *consumed_ptr = q;
+        }
+        if (lane == 0 && best) atomicMax(&sbest[full_vocab ? 0 : cur], best);
+        cons_sync();
+        if (tid < b_count) {
+            if (sbest[tid]) atomicMax(&p.keys[(size_t)(b_first + tid) * kBlock + k], sbest[tid]);
+            sbest[tid] = 0ull;
+        }
+    };
+
+    // base-logit values of step k for the slice, fetched asynchronously
+    auto prefetch_L = [&](int k) {
+        if (full_vocab) {
+            for (int i = tid; i < B * nw; i += kConsumerWarps * 32) {
+                const int b = i / nw, r = i % nw;
+                cp_async4(&sL[b * p.seg + r], p.L + ((size_t)b * kBlock + kRowOffset + k) * V + w0 + r);
+            }
+        } else {
+            for (int r = tid; r < nw; r += kConsumerWarps * 32) {
+                const long long item = w0 + r;
+                const int b = (int)(item / p.K);
+                cp_async4(&sL[r], p.L + ((size_t)b * kBlock + kRowOffset + k) * V + p.pool[item]);
+            }
+        }
+        cp_async_commit();
+    };
+
+    gru(0);
+    if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+    gru(1);
+    if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+    for (int k = 1; k <= kCorrected; ++k) {
+        prefetch_L(k);
+        fc1(k);
+        if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+        correct(k);
+        if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+        if (k < kCorrected) {
+            gru(k + 1);
+            if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
+    const domino_config& g = c->cfg;
+    const int grid = c->num_sms;
+    const bool full_vocab = r.K == 0;
+    const long long work = full_vocab ? (long long)g.V : (long long)r.B * r.K;
+    int seg = (int)((work + grid - 1) / grid);
+    seg = (seg + kRowsPerSlot - 1) / kRowsPerSlot * kRowsPerSlot;
+    const int row_bytes = g.F * (int)sizeof(T);
+    const int slot_bytes = kRowsPerSlot * row_bytes;
+    // ring gets what the rest of the layout leaves of the opt-in maximum
+    int max_smem = 0;
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    Layout base(0, slot_bytes, g.E, g.G, g.F, seg, r.B);
+    int n_slots = (max_smem - base.total - 1024) / (slot_bytes + 16);
+    if (n_slots > 12) n_slots = 12;
+    if (n_slots < 2) return cudaErrorNotSupported;
+    Layout lay(n_slots, slot_bytes, g.E, g.G, g.F, seg, r.B);
+
+    PersistParams<T> p;
+    p.emb = (const T*)c->emb;
+    p.w_ih = (const T*)c->w_ih;
+    p.w_hh = (const T*)c->w_hh;
+    p.fc1 = (const T*)c->fc1;
+    p.fc2 = (const T*)c->fc2;
+    p.bias = (const T*)c->bias;
+    p.s = (const T*)r.s;
+    p.verified = r.verified;
+    p.forced = r.forced;
+    p.pool = c->pool;
+    p.L = c->L;
+    p.h = c->h;
+    p.a = c->a;
+    p.keys = c->keys;
+    p.bad = c->bad;
+    p.err = c->err;
+    p.sync = c->sync;
+    p.dbg_h = r.dbg.h;
+    p.dbg_z = r.dbg.z;
+    p.dbg_scores = r.dbg.scores;
+    p.B = r.B;
+    p.K = r.K;
+    p.V = g.V;
+    p.E = g.E;
+    p.G = g.G;
+    p.F = g.F;
+    p.max_B = g.max_B;
+    p.seg = seg;
+    p.n_slots = n_slots;
+    p.slot_bytes = slot_bytes;
+
+    auto kern = k_rollout_persist<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPersistThreads);
+    cfg.dynamicSmemBytes = lay.total;
+    cfg.stream = r.st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    ++r.launches;
+    return e;
+}
+
+}  // namespace
+
+// Whether the persistent driver covers this run: one request over the full
+// vocabulary, or a pool whose per-CTA slice touches at most kMaxReq requests;
+// rows must be whole 16-byte units and the per-CTA slice must fit the tables.
+bool persist_supported(const domino_ctx* c, const RunArgs& r) {
+    const domino_config& g = c->cfg;
+    const int esize = g.dtype == DOMINO_DTYPE_BF16 ? 2 : 4;
+    if (((g.E | g.G | g.F) & 7) || (g.F * esize) % 16 != 0 || g.F > 2048 || g.E > 2048 || g.G > 2048) return false;
+    if ((g.G + c->num_sms - 1) / c->num_sms > 64) return false;
+    if (r.B > 256) return false;
+    const int grid = c->num_sms;
+    if (r.K == 0) {
+        if (r.B != 1) return false;
+        const int seg = (g.V + grid - 1) / grid;
+        return seg + kRowsPerSlot <= kMaxSeg;
+    }
+    const long long work = (long long)r.B * r.K;
+    const long long seg = (work + grid - 1) / grid + kRowsPerSlot;
+    if (seg > kMaxSeg) return false;
+    return seg / r.K + 2 <= kMaxReq;
+}
+
+cudaError_t launch_persist(domino_ctx* c, RunArgs& r) {
+    return c->cfg.dtype == DOMINO_DTYPE_BF16 ? launch_t<__nv_bfloat16>(c, r) : launch_t<float>(c, r);
+}
+
+}  // namespace domino
