@@ -76,9 +76,11 @@ def alg_bytes(sh: inputs.Shape, B: int, K: int) -> dict:
     gru = 3 * G * (E + G) * e + B * (E * e + G * 4 * 2)
     fc1 = F * G * e + B * (G * 4 + F * e + F * 4 * 2)
     pool = 0 if full else B * 15 * V * 4 + B * V * 4 * 5 + B * K * 4
-    per_block = lm + V * 0 + pool + 15 * gru + 14 * (fc1 + corr)
-    return {"lmhead": lm, "correct": corr, "gru": gru, "fc1": fc1, "pool": pool, "block": per_block,
-            "lmhead_flop": 2.0 * B * 16 * V * H}
+    # persistent driver: the GRU seed and 14 corrected steps in one launch
+    steps = 15 * gru + 14 * (fc1 + corr)
+    per_block = lm + pool + steps
+    return {"lmhead": lm, "correct": corr, "gru": gru, "fc1": fc1, "pool": pool, "steps": steps,
+            "block": per_block, "lmhead_flop": 2.0 * B * 16 * V * H}
 
 
 # ---- clocks sampler ---------------------------------------------------------

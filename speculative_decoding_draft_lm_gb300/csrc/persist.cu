@@ -108,11 +108,18 @@ __device__ __forceinline__ void lds8(const __nv_bfloat16* p, float* o) {
 }
 
 // Shared-memory layout (bytes, all offsets 128-aligned)
+// Requests whose activations one CTA needs in phase C.
+__host__ __device__ inline int phase_c_requests(int B, int K, int seg) {
+    if (K == 0) return B;
+    const int n = seg / K + 2;
+    return n < B ? n : B;
+}
+
 struct Layout {
     int ring, bars, sa, sx, sh, sg, sL, sbias, sbest, stok, misc, total;
-    __host__ __device__ Layout(int n_slots, int slot_bytes, int E, int G, int F, int seg, int B) {
+    __host__ __device__ Layout(int n_slots, int slot_bytes, int E, int G, int F, int seg, int B, int K) {
         auto up = [](int x) { return (x + 127) & ~127; };
-        const int nreq = B < kMaxReq ? B : kMaxReq, ngru = B < kGruGroup ? B : kGruGroup;
+        const int nreq = phase_c_requests(B, K, seg), ngru = B < kGruGroup ? B : kGruGroup;
         int o = 0;
         ring = o; o = up(o + n_slots * slot_bytes);
         bars = o; o = up(o + 16 * n_slots);
@@ -120,7 +127,7 @@ struct Layout {
         sx = o;   o = up(o + 4 * ngru * E);
         sh = o;   o = up(o + 4 * ngru * G);
         sg = o;   o = up(o + 4 * 6 * kGruGroup * 64);   // gate pre-activations of <= 64 outputs
-        sL = o;   o = up(o + 4 * seg * nreq);
+        sL = o;   o = up(o + 4 * seg * (K == 0 ? nreq : 1));
         sbias = o; o = up(o + 4 * seg);
         sbest = o; o = up(o + 8 * kMaxReq);
         stok = o; o = up(o + 4 * 256);
@@ -132,7 +139,7 @@ struct Layout {
 template <typename T>
 __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistParams<T> p) {
     extern __shared__ __align__(128) uint8_t sm[];
-    const Layout lay(p.n_slots, p.slot_bytes, p.E, p.G, p.F, p.seg, p.B);
+    const Layout lay(p.n_slots, p.slot_bytes, p.E, p.G, p.F, p.seg, p.B, p.K);
     uint8_t* ring = sm + lay.ring;
     const uint32_t full0 = tc::smem_u32(sm + lay.bars), empty0 = full0 + 8 * p.n_slots;
     float* sa = reinterpret_cast<float*>(sm + lay.sa);
@@ -486,24 +493,40 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     }
 }
 
+struct Plan {
+    int seg, slot_bytes, n_slots, smem;
+};
+
+// Per-CTA slice, ring slot size and ring depth: the ring gets what the rest
+// of the layout leaves of the opt-in shared-memory maximum (n_slots < 2: no).
+Plan make_plan(const domino_ctx* c, int B, int K) {
+    const domino_config& g = c->cfg;
+    const int grid = c->num_sms;
+    const long long work = K == 0 ? (long long)g.V : (long long)B * K;
+    int seg = (int)((work + grid - 1) / grid);
+    seg = (seg + kRowsPerSlot - 1) / kRowsPerSlot * kRowsPerSlot;
+    const int esize = g.dtype == DOMINO_DTYPE_BF16 ? 2 : 4;
+    const int slot_bytes = kRowsPerSlot * g.F * esize;
+    int max_smem = 0;
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    Layout base(0, slot_bytes, g.E, g.G, g.F, seg, B, K);
+    int n_slots = (max_smem - base.total - 1024) / (slot_bytes + 16);
+    if (n_slots > 12) n_slots = 12;
+    Plan pl{seg, slot_bytes, n_slots, 0};
+    if (n_slots >= 2) pl.smem = Layout(n_slots, slot_bytes, g.E, g.G, g.F, seg, B, K).total;
+    return pl;
+}
+
 template <typename T>
 cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     const domino_config& g = c->cfg;
     const int grid = c->num_sms;
-    const bool full_vocab = r.K == 0;
-    const long long work = full_vocab ? (long long)g.V : (long long)r.B * r.K;
-    int seg = (int)((work + grid - 1) / grid);
-    seg = (seg + kRowsPerSlot - 1) / kRowsPerSlot * kRowsPerSlot;
-    const int row_bytes = g.F * (int)sizeof(T);
-    const int slot_bytes = kRowsPerSlot * row_bytes;
-    // ring gets what the rest of the layout leaves of the opt-in maximum
-    int max_smem = 0;
-    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
-    Layout base(0, slot_bytes, g.E, g.G, g.F, seg, r.B);
-    int n_slots = (max_smem - base.total - 1024) / (slot_bytes + 16);
-    if (n_slots > 12) n_slots = 12;
-    if (n_slots < 2) return cudaErrorNotSupported;
-    Layout lay(n_slots, slot_bytes, g.E, g.G, g.F, seg, r.B);
+    const Plan pl = make_plan(c, r.B, r.K);
+    if (pl.n_slots < 2) return cudaErrorNotSupported;
+    const int seg = pl.seg, slot_bytes = pl.slot_bytes, n_slots = pl.n_slots;
+    struct {
+        int total;
+    } lay{pl.smem};
 
     PersistParams<T> p;
     p.emb = (const T*)c->emb;
@@ -570,12 +593,13 @@ bool persist_supported(const domino_ctx* c, const RunArgs& r) {
     if (r.K == 0) {
         if (r.B != 1) return false;
         const int seg = (g.V + grid - 1) / grid;
-        return seg + kRowsPerSlot <= kMaxSeg;
+        return seg + kRowsPerSlot <= kMaxSeg && make_plan(c, r.B, r.K).n_slots >= 2;
     }
     const long long work = (long long)r.B * r.K;
     const long long seg = (work + grid - 1) / grid + kRowsPerSlot;
     if (seg > kMaxSeg) return false;
-    return seg / r.K + 2 <= kMaxReq;
+    if (seg / r.K + 2 > kMaxReq && r.B > kMaxReq) return false;
+    return make_plan(c, r.B, r.K).n_slots >= 2;
 }
 
 cudaError_t launch_persist(domino_ctx* c, RunArgs& r) {
