@@ -396,6 +396,7 @@ def main():
             eng.enable_timing(True)
             eng.read_timing()
             lm_ms, lm_n = 0.0, 0
+            ph_ms = {}
             for _ in range(max(5, args.steps // 2)):
                 flush.zero_()
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -408,6 +409,9 @@ def main():
                 ph = eng.read_timing()
                 lm_ms += ph["lmhead"][0]
                 lm_n += ph["lmhead"][1]
+                for k_, (m_, n_) in ph.items():
+                    if n_:
+                        ph_ms[k_] = ph_ms.get(k_, 0.0) + m_
             eng.enable_timing(False)
             ms = sum(tt) / len(tt)
             ab2 = alg_bytes(sh, w2.B, w2.K)
@@ -415,7 +419,8 @@ def main():
             table[name] = {"us_per_block": ms * 1e3, "proposals_per_s": 15.0 * w2.B / (ms * 1e-3),
                            "hbm_frac_block": ab2["block"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "lmhead_us": lm_avg * 1e3,
-                           "lmhead_tensor_frac": ab2["lmhead_flop"] / (lm_avg * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+                           "lmhead_tensor_frac": ab2["lmhead_flop"] / (lm_avg * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                           "phase_us": {k_: m_ * 1e3 / len(tt) for k_, m_ in ph_ms.items()}}
         torch.cuda.synchronize()
         if eng.status() != 0:
             raise RuntimeError("device error during the sweep")

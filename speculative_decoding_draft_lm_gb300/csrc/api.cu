@@ -114,8 +114,11 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     if (use_persist) {
         STEP(DOMINO_PHASE_STEPS, launch_persist(c, r));
     } else {
-    STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 0));
-    STEP(DOMINO_PHASE_GRU, launch_gru(c, r, 1));
+    const bool batch = r.B >= 2 && batch_kernels_supported(c);
+#define GRU(u) (batch ? launch_gru_batch(c, r, (u)) : launch_gru(c, r, (u)))
+#define FC1(k) (batch ? launch_fc1_batch(c, r, (k)) : launch_fc1(c, r, (k)))
+    STEP(DOMINO_PHASE_GRU, GRU(0));
+    STEP(DOMINO_PHASE_GRU, GRU(1));
     {
         // tensor cores once the full-vocabulary correction is a real
         // contraction (two or more requests); CUDA cores for B = 1 and pools
@@ -126,14 +129,16 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
             if (e != cudaSuccess) goto fail;
         }
         for (int k = 1; k <= kCorrected; ++k) {
-            STEP(DOMINO_PHASE_FC1, launch_fc1(c, r, k));
+            STEP(DOMINO_PHASE_FC1, FC1(k));
             if (tc_corr)
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_tc(c, r, tm_a, k));
             else
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
-            if (k < kCorrected) STEP(DOMINO_PHASE_GRU, launch_gru(c, r, k + 1));
+            if (k < kCorrected) STEP(DOMINO_PHASE_GRU, GRU(k + 1));
         }
     }
+#undef GRU
+#undef FC1
     }
     STEP(DOMINO_PHASE_OTHER, launch_finalize(c, r));
     if (r.dbg.logits)

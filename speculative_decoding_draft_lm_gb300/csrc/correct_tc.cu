@@ -35,14 +35,20 @@ struct EpiCorrect {
                                                unsigned long long* sb) const {
         if (col0 >= B) return;  // uniform: padding columns
         const bool ok = row < V;
+        const int nb = B - col0 < 16 ? B - col0 : 16;
+        // all base-logit loads of the chunk are in flight before any is used
+        float base[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            base[j] = (ok && j < nb) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
         const float bv = ok ? __bfloat162float(bias[row]) : 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int b = col0 + j;
-            if (b >= B) break;  // uniform
+            if (j >= nb) break;  // uniform
             float c = 0.f;
             if (ok) {
-                c = v[j] + bv + L[((size_t)b * kBlock + kRowOffset + k) * V + row];
+                c = v[j] + bv + base[j];
                 if (dbg_scores) dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + row] = c;
             }
             unsigned long long key = ok ? pack_key(c, (uint32_t)row) : 0ull;

@@ -42,6 +42,15 @@ bool correct_tc_supported(const domino_ctx* c, const RunArgs& r);
 cudaError_t prepare_correct_tc(domino_ctx* c, RunArgs& r, CUtensorMap* tmB);
 cudaError_t launch_correct_tc(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k);
 
+// cluster radix-select candidate pool (pool.cu)
+bool pool_cluster_supported(const domino_ctx* c);
+cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r);
+
+// batched GRU / projector layer 1 for B >= 2 (kernels_batch.cu)
+bool batch_kernels_supported(const domino_ctx* c);
+cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u);
+cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k);
+
 // persistent driver of the GRU seed and the 14 corrected steps (persist.cu)
 bool persist_supported(const domino_ctx* c, const RunArgs& r);
 cudaError_t launch_persist(domino_ctx* c, RunArgs& r);

@@ -1,0 +1,275 @@
+// Batched GRU update and projector layer 1 for several requests at once
+// (the per-phase driver with B >= 2).
+//
+// GRU (page "Add correctness-first Domino support to DFlash V2", section
+// "Design": bias-free GRU; gate rows r|z|n, PyTorch GRUCell algebra):
+//   r = sigmoid(W_ir x + W_hr h), u = sigmoid(W_iz x + W_hz h),
+//   n = tanh(W_in x + r * (W_hn h)), h' = (1 - u) * n + u * h.
+// Projector layer 1 (page "[Spec] Add Domino projector support to DFlash
+// speculative decoding (V2)", section "Implementation"): a = SiLU(fc1 h + s).
+//
+// Layout: a CTA owns JT consecutive state elements j (3 gate rows of W_ih
+// and of W_hh each), staged once in shared memory; each warp takes requests
+// in turn, holds the request's embedding row and state in registers (lane l
+// owns elements (l + 32c)*8 .. +7) and forms all 6*JT dot products from them.
+#include "internal.h"
+
+namespace domino {
+
+namespace {
+
+constexpr int kJT = 4;        // GRU state elements per CTA
+constexpr int kFT = 8;        // projector outputs per CTA
+constexpr int kBatchThreads = 256;
+
+template <typename T, int NCH>
+struct VecRegs {
+    float v[NCH][8];
+    __device__ __forceinline__ void load_t(const T* p, int n, int lane) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int e = (lane + 32 * c) * 8;
+            if (e < n) load8(p + e, v[c]);
+            else
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[c][i] = 0.f;
+        }
+    }
+    __device__ __forceinline__ void load_f(const float* p, int n, int lane) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int e = (lane + 32 * c) * 8;
+            if (e < n) {
+                const float4 x = *reinterpret_cast<const float4*>(p + e);
+                const float4 y = *reinterpret_cast<const float4*>(p + e + 4);
+                v[c][0] = x.x; v[c][1] = x.y; v[c][2] = x.z; v[c][3] = x.w;
+                v[c][4] = y.x; v[c][5] = y.y; v[c][6] = y.z; v[c][7] = y.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[c][i] = 0.f;
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ void sm8(const float* p, float* o) {
+    const float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+}
+__device__ __forceinline__ void sm8(const __nv_bfloat16* p, float* o) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    bf16x2_to_f32(q.x, o[0], o[1]);
+    bf16x2_to_f32(q.y, o[2], o[3]);
+    bf16x2_to_f32(q.z, o[4], o[5]);
+    bf16x2_to_f32(q.w, o[6], o[7]);
+}
+
+// lane-partial dot of a shared-memory row with register-resident elements
+template <typename T, int NCH>
+__device__ __forceinline__ float part_dot(const T* row, const VecRegs<T, NCH>& x, int n, int lane) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int e = (lane + 32 * c) * 8;
+        if (e < n) {
+            float w[8];
+            sm8(row + e, w);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                a0 = fmaf(w[i], x.v[c][i], a0);
+                a1 = fmaf(w[i + 1], x.v[c][i + 1], a1);
+            }
+        }
+    }
+    return a0 + a1;
+}
+
+// 16-byte asynchronous global -> shared copies: every copy of a staging loop
+// is in flight at once (no register round trip); cp_wait() completes them.
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_all;" ::: "memory");
+}
+
+// Stage gate rows: for gate g < 3 and jj < nrows, source row
+// g*gate_rows + row0 + jj (n elements) -> shared row g*nrows + jj.
+template <typename T>
+__device__ __forceinline__ void stage_rows(T* dst, const T* src_base, int row0, int nrows, int gate_rows, int n) {
+    const int per_row = n * (int)sizeof(T) / 16;
+    for (int i = threadIdx.x; i < 3 * nrows * per_row; i += blockDim.x) {
+        const int rr = i / per_row, e = (i % per_row) * (16 / (int)sizeof(T));
+        const int g = rr / nrows, jj = rr % nrows;
+        cp16(dst + (size_t)rr * n + e, src_base + (size_t)(g * gate_rows + row0 + jj) * n + e);
+    }
+}
+
+template <typename T, int NCH>
+__global__ void __launch_bounds__(kBatchThreads) k_gru_batch(
+    const T* __restrict__ emb, const T* __restrict__ w_ih, const T* __restrict__ w_hh, const float* __restrict__ h_in,
+    float* __restrict__ h_out, const int32_t* __restrict__ verified, const int32_t* __restrict__ forced,
+    const unsigned long long* __restrict__ keys, int* __restrict__ bad, int* __restrict__ err,
+    float* __restrict__ dbg_h, int u, int B, int V, int E, int G) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int j0 = blockIdx.x * kJT;
+    const int jn = min(kJT, G - j0);
+    T* s_ih = reinterpret_cast<T*>(smem);                      // [3*jn][E]
+    T* s_hh = s_ih + (size_t)3 * kJT * E;                      // [3*jn][G]
+    stage_rows(s_ih, w_ih, j0, jn, G, E);
+    if (u > 0) stage_rows(s_hh, w_hh, j0, jn, G, G);
+    cp_wait();
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = warp; b < B; b += kBatchThreads / 32) {
+        int t;
+        if (u == 0) t = verified[b];
+        else if (forced) t = forced[(size_t)b * kProposals + (u - 1)];
+        else t = (int)key_index(keys[(size_t)b * kBlock + (u - 1)]);
+        if (t < 0 || t >= V) {
+            if (blockIdx.x == 0 && lane == 0) {
+                bad[b] = 1;
+                atomicOr(err, kErrBadToken);
+            }
+            t = 0;
+        }
+        VecRegs<T, NCH> x;
+        x.load_t(emb + (size_t)t * E, E, lane);
+        VecRegs<T, NCH> hv;
+        if (u > 0) hv.load_f(h_in + (size_t)b * G, G, lane);
+        float gi[3 * kJT], gh[3 * kJT];
+#pragma unroll
+        for (int i = 0; i < 3 * kJT; ++i) {
+            gi[i] = 0.f;
+            gh[i] = 0.f;
+            if (i / kJT < 3 && (i % kJT) < jn) {
+                const int g = i / kJT, jj = i % kJT;
+                gi[i] = warp_sum(part_dot(s_ih + (size_t)(g * jn + jj) * E, x, E, lane));
+                if (u > 0) gh[i] = warp_sum(part_dot(s_hh + (size_t)(g * jn + jj) * G, hv, G, lane));
+            }
+        }
+        if (lane < jn) {
+            float ir = 0, iz = 0, in_ = 0, hr = 0, hz = 0, hn = 0;
+#pragma unroll
+            for (int jj = 0; jj < kJT; ++jj)
+                if (jj == lane) {
+                    ir = gi[0 * kJT + jj]; iz = gi[1 * kJT + jj]; in_ = gi[2 * kJT + jj];
+                    hr = gh[0 * kJT + jj]; hz = gh[1 * kJT + jj]; hn = gh[2 * kJT + jj];
+                }
+            const int j = j0 + lane;
+            const float r = sigmoidf_(ir + hr);
+            const float zg = sigmoidf_(iz + hz);
+            const float n = tanhf(in_ + r * hn);
+            const float hp = u > 0 ? h_in[(size_t)b * G + j] : 0.f;
+            const float out = (1.f - zg) * n + zg * hp;
+            h_out[(size_t)b * G + j] = out;
+            if (dbg_h) dbg_h[((size_t)b * kProposals + u) * G + j] = out;
+        }
+    }
+}
+
+template <typename T, int NCH>
+__global__ void __launch_bounds__(kBatchThreads) k_fc1_batch(const T* __restrict__ fc1, const float* __restrict__ h,
+                                                             const T* __restrict__ s, float* __restrict__ a,
+                                                             __nv_bfloat16* __restrict__ a16, float* __restrict__ dbg_z,
+                                                             int k, int B, int G, int F) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int f0 = blockIdx.x * kFT;
+    const int fn = min(kFT, F - f0);
+    T* s_w = reinterpret_cast<T*>(smem);  // [fn][G]
+    const int per_row = G * (int)sizeof(T) / 16;
+    for (int i = threadIdx.x; i < fn * per_row; i += blockDim.x) {
+        const int rr = i / per_row, e = (i % per_row) * (16 / (int)sizeof(T));
+        cp16(s_w + (size_t)rr * G + e, fc1 + (size_t)(f0 + rr) * G + e);
+    }
+    cp_wait();
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = warp; b < B; b += kBatchThreads / 32) {
+        VecRegs<T, NCH> hv;
+        hv.load_f(h + (size_t)b * G, G, lane);
+        float z[kFT];
+#pragma unroll
+        for (int i = 0; i < kFT; ++i) z[i] = i < fn ? warp_sum(part_dot(s_w + (size_t)i * G, hv, G, lane)) : 0.f;
+        if (lane < fn) {
+            float zz = 0.f;
+#pragma unroll
+            for (int i = 0; i < kFT; ++i)
+                if (i == lane) zz = z[i];
+            const int f = f0 + lane;
+            zz += to_f32(s[((size_t)b * kProposals + k) * F + f]);
+            const float act = zz * sigmoidf_(zz);
+            a[(size_t)b * F + f] = act;
+            a16[(size_t)b * F + f] = __float2bfloat16_rn(act);
+            if (dbg_z) dbg_z[((size_t)b * kCorrected + (k - 1)) * F + f] = zz;
+        }
+    }
+}
+
+template <typename T>
+using GruKern = void (*)(const T*, const T*, const T*, const float*, float*, const int32_t*, const int32_t*,
+                         const unsigned long long*, int*, int*, float*, int, int, int, int, int);
+template <typename T>
+using Fc1Kern = void (*)(const T*, const float*, const T*, float*, __nv_bfloat16*, float*, int, int, int, int);
+
+template <typename T>
+GruKern<T> pick_gru(int nch) {
+    return nch <= 1 ? k_gru_batch<T, 1> : nch <= 2 ? k_gru_batch<T, 2> : nch <= 4 ? k_gru_batch<T, 4>
+         : nch <= 6 ? k_gru_batch<T, 6> : nch <= 8 ? k_gru_batch<T, 8> : nullptr;
+}
+template <typename T>
+Fc1Kern<T> pick_fc1(int nch) {
+    return nch <= 1 ? k_fc1_batch<T, 1> : nch <= 2 ? k_fc1_batch<T, 2> : nch <= 4 ? k_fc1_batch<T, 4>
+         : nch <= 6 ? k_fc1_batch<T, 6> : nch <= 8 ? k_fc1_batch<T, 8> : nullptr;
+}
+
+inline int nch_of(int n) { return (n + 255) / 256; }
+
+}  // namespace
+
+bool batch_kernels_supported(const domino_ctx* c) {
+    const domino_config& g = c->cfg;
+    if (g.dtype != DOMINO_DTYPE_BF16) return false;
+    if ((g.E | g.G | g.F) & 7) return false;
+    const int mx = g.E > g.G ? (g.E > g.F ? g.E : g.F) : (g.G > g.F ? g.G : g.F);
+    if (nch_of(mx) > 8) return false;
+    const size_t gru_smem = (size_t)3 * kJT * (g.E + g.G) * 2;
+    return gru_smem <= 200 * 1024;
+}
+
+cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u) {
+    using T = __nv_bfloat16;
+    const domino_config& g = c->cfg;
+    const float* h_in = c->h + (size_t)h_slot(u + 1) * g.max_B * g.G;
+    float* h_out = c->h + (size_t)h_slot(u) * g.max_B * g.G;
+    const int mx = g.E > g.G ? g.E : g.G;
+    GruKern<T> kern = pick_gru<T>(nch_of(mx));
+    const size_t smem = (size_t)3 * kJT * (g.E + g.G) * sizeof(T);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = (g.G + kJT - 1) / kJT;
+    kern<<<grid, kBatchThreads, smem, r.st>>>((const T*)c->emb, (const T*)c->w_ih, (const T*)c->w_hh, h_in, h_out,
+                                              r.verified, r.forced, c->keys, c->bad, c->err, r.dbg.h, u, r.B, g.V,
+                                              g.E, g.G);
+    ++r.launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k) {
+    using T = __nv_bfloat16;
+    const domino_config& g = c->cfg;
+    const float* h = c->h + (size_t)h_slot(k) * g.max_B * g.G;
+    Fc1Kern<T> kern = pick_fc1<T>(nch_of(g.G));
+    const size_t smem = (size_t)kFT * g.G * sizeof(T);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = (g.F + kFT - 1) / kFT;
+    kern<<<grid, kBatchThreads, smem, r.st>>>((const T*)c->fc1, h, (const T*)r.s, c->a, c->a16, r.dbg.z, k, r.B,
+                                              g.G, g.F);
+    ++r.launches;
+    return cudaGetLastError();
+}
+
+}  // namespace domino

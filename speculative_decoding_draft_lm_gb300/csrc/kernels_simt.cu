@@ -431,6 +431,7 @@ cudaError_t launch_pool_select(domino_ctx* c, RunArgs& r, bool score_ready) {
         k_score<<<grid, 256, 0, r.st>>>(c->L, c->score, r.B, c->cfg.V);
         DOMINO_LAUNCH_CHECK();
     }
+    if (pool_cluster_supported(c)) return launch_pool_cluster(c, r);
     k_pool_select<<<r.B, 1024, 0, r.st>>>(c->score, c->pool, c->cfg.V, r.K);
     DOMINO_LAUNCH_CHECK();
     return cudaSuccess;

@@ -32,9 +32,10 @@ namespace domino {
 
 namespace {
 
-constexpr int kConsumerWarps = 16;
+// 15 consumer warps + 1 producer warp: 16 warps leave 128 registers a thread
+constexpr int kConsumerWarps = 15;
 constexpr int kPersistThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRowsPerSlot = 16;   // one row per consumer warp per slot
+constexpr int kRowsPerSlot = kConsumerWarps;  // one row per consumer warp per slot
 constexpr int kMaxReq = 8;         // requests a CTA may touch in phase C
 constexpr int kGruGroup = 4;       // requests per GRU/fc1 staging group
 constexpr int kMaxSeg = 2048;      // rows (or pool entries) per CTA
@@ -56,7 +57,7 @@ struct PersistParams {
     int slot_bytes;
 };
 
-__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     unsigned v;
@@ -70,8 +71,7 @@ __device__ bool grid_sync(unsigned* counter, unsigned& n, volatile int* abort_fl
     cons_sync();
     ++n;
     if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(counter, 1u);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
         const unsigned target = n * gridDim.x;
         const unsigned long long t0 = tc::globaltimer();
         while (ld_acquire(counter) < target) {
@@ -82,7 +82,6 @@ __device__ bool grid_sync(unsigned* counter, unsigned& n, volatile int* abort_fl
                 break;
             }
         }
-        __threadfence();
     }
     cons_sync();
     return !*abort_flag;
@@ -107,6 +106,80 @@ __device__ __forceinline__ void lds8(const __nv_bfloat16* p, float* o) {
     bf16x2_to_f32(q.w, o[6], o[7]);
 }
 
+// One weight row held in registers: lane l owns elements (l + 32 c) * 8 .. +7
+// for c < NCH (NCH * 256 >= row length).  All chunks are requested before any
+// is used, with an L2 evict-last hint (these small matrices are re-read every
+// step while fc2 streams past them).
+template <typename T, int NCH>
+struct RegRow;
+template <int NCH>
+struct RegRow<__nv_bfloat16, NCH> {
+    uint4 q[NCH];
+    __device__ __forceinline__ void load(const __nv_bfloat16* row, int n, int lane, uint64_t pol) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int e = (lane + 32 * c) * 8;
+            if (e < n)
+                asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                             : "=r"(q[c].x), "=r"(q[c].y), "=r"(q[c].z), "=r"(q[c].w)
+                             : "l"(row + e), "l"(pol));
+            else
+                q[c] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    __device__ __forceinline__ void get(int c, float* o) const {
+        bf16x2_to_f32(q[c].x, o[0], o[1]);
+        bf16x2_to_f32(q[c].y, o[2], o[3]);
+        bf16x2_to_f32(q[c].z, o[4], o[5]);
+        bf16x2_to_f32(q[c].w, o[6], o[7]);
+    }
+};
+template <int NCH>
+struct RegRow<float, NCH> {
+    float4 q[2 * NCH];
+    __device__ __forceinline__ void load(const float* row, int n, int lane, uint64_t pol) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int e = (lane + 32 * c) * 8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (e < n)
+                    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                                 : "=f"(q[2 * c + h].x), "=f"(q[2 * c + h].y), "=f"(q[2 * c + h].z),
+                                   "=f"(q[2 * c + h].w)
+                                 : "l"(row + e + 4 * h), "l"(pol));
+                else
+                    q[2 * c + h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+    __device__ __forceinline__ void get(int c, float* o) const {
+        o[0] = q[2 * c].x; o[1] = q[2 * c].y; o[2] = q[2 * c].z; o[3] = q[2 * c].w;
+        o[4] = q[2 * c + 1].x; o[5] = q[2 * c + 1].y; o[6] = q[2 * c + 1].z; o[7] = q[2 * c + 1].w;
+    }
+};
+
+// dot of a register row with a shared-memory fp32 vector (same element map)
+template <typename T, int NCH>
+__device__ __forceinline__ float row_dot_smem(const RegRow<T, NCH>& w, const float* x, int n, int lane) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int e = (lane + 32 * c) * 8;
+        if (e < n) {
+            float ww[8], xx[8];
+            w.get(c, ww);
+            lds8(x + e, xx);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                a0 = fmaf(ww[i], xx[i], a0);
+                a1 = fmaf(ww[i + 1], xx[i + 1], a1);
+            }
+        }
+    }
+    return a0 + a1;
+}
+
 // Shared-memory layout (bytes, all offsets 128-aligned)
 // Requests whose activations one CTA needs in phase C.
 __host__ __device__ inline int phase_c_requests(int B, int K, int seg) {
@@ -126,8 +199,8 @@ struct Layout {
         sa = o;   o = up(o + 4 * nreq * F);
         sx = o;   o = up(o + 4 * ngru * E);
         sh = o;   o = up(o + 4 * ngru * G);
-        sg = o;   o = up(o + 4 * 6 * kGruGroup * 64);   // gate pre-activations of <= 64 outputs
-        sL = o;   o = up(o + 4 * seg * (K == 0 ? nreq : 1));
+        sg = o;   o = up(o + 4 * 9 * kGruGroup * 64);   // gate products + next hidden-side products
+        sL = o;   o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
         sbest = o; o = up(o + 8 * kMaxReq);
         stok = o; o = up(o + 4 * 256);
@@ -136,7 +209,7 @@ struct Layout {
     }
 };
 
-template <typename T>
+template <typename T, int NCH>
 __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistParams<T> p) {
     extern __shared__ __align__(128) uint8_t sm[];
     const Layout lay(p.n_slots, p.slot_bytes, p.E, p.G, p.F, p.seg, p.B, p.K);
@@ -244,8 +317,16 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     const int fpc = (F + gridDim.x - 1) / gridDim.x;
     const int f0 = min(F, (int)blockIdx.x * fpc), f1 = min(F, f0 + fpc);
 
-    // ---- one GRU update u for every request; writes h[slot(u)]
-    auto gru = [&](int u) {
+    const uint64_t pol_keep = tc::policy_evict_last();
+    // W_hh h of the next GRU update is computed during the correction phase
+    // (its warps have slack while fc2 streams) when all requests fit one group
+    const bool pre_gh = B <= kGruGroup;
+    float* sgh = sg + 6 * kGruGroup * 64;  // [kGruGroup][64][3], after the gate products
+
+    // ---- one GRU update u for every request; writes h[slot(u)].  With
+    // gh_ready, the hidden-side products are in sgh and h_in is still staged
+    // in sh (it was staged for the projector of the same step).
+    auto gru = [&](int u, bool gh_ready) {
         const float* h_in = p.h + (size_t)h_slot(u + 1) * p.max_B * G;
         float* h_out = p.h + (size_t)h_slot(u) * p.max_B * G;
         if (tid < B) {
@@ -262,59 +343,44 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             }
             stok[tid] = t;
         }
-        cons_sync();
+        const bool need_gh = u > 0 && !gh_ready;
         for (int g0 = 0; g0 < B; g0 += kGruGroup) {
             const int ng = min(kGruGroup, B - g0);
+            // first item's weight rows are requested before the staging loads
+            RegRow<T, NCH> wi, wh;
+            int it = warp;
+            if (it < jn * 3) {
+                const int jj = it / 3, gate = it % 3;
+                wi.load(p.w_ih + (size_t)(gate * G + j0 + jj) * E, E, lane, pol_keep);
+                if (need_gh) wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
+            }
+            cons_sync();  // stok visible
             for (int i = tid; i < ng * E; i += kConsumerWarps * 32) {
                 const int b = i / E, e = i % E;
                 sx[b * E + e] = to_f32(p.emb[(size_t)stok[g0 + b] * E + e]);
             }
-            if (u > 0)
+            if (u > 0 && !gh_ready)
                 for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
                     const int b = i / G, e = i % G;
                     sh[b * G + e] = __ldcg(&h_in[(size_t)(g0 + b) * G + e]);
                 }
             cons_sync();
-            // one warp per (output j, gate): input and hidden dot products
-            for (int it = warp; it < jn * 3; it += kConsumerWarps) {
+            for (; it < jn * 3; it += kConsumerWarps) {
                 const int jj = it / 3, gate = it % 3;
-                const T* wi = p.w_ih + (size_t)(gate * G + j0 + jj) * E;
-                const T* wh = p.w_hh + (size_t)(gate * G + j0 + jj) * G;
-                float gi[kGruGroup], gh[kGruGroup];
-#pragma unroll
-                for (int b = 0; b < kGruGroup; ++b) gi[b] = gh[b] = 0.f;
-                for (int e = lane * 8; e < E; e += 256) {
-                    float w[8];
-                    load8(wi + e, w);
-#pragma unroll
-                    for (int b = 0; b < kGruGroup; ++b)
-                        if (b < ng) {
-                            float x[8];
-                            lds8(sx + b * E + e, x);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) gi[b] = fmaf(w[q], x[q], gi[b]);
-                        }
+                if (it != warp) {
+                    wi.load(p.w_ih + (size_t)(gate * G + j0 + jj) * E, E, lane, pol_keep);
+                    if (need_gh) wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
                 }
-                if (u > 0)
-                    for (int e = lane * 8; e < G; e += 256) {
-                        float w[8];
-                        load8(wh + e, w);
-#pragma unroll
-                        for (int b = 0; b < kGruGroup; ++b)
-                            if (b < ng) {
-                                float x[8];
-                                lds8(sh + b * G + e, x);
-#pragma unroll
-                                for (int q = 0; q < 8; ++q) gh[b] = fmaf(w[q], x[q], gh[b]);
-                            }
-                    }
 #pragma unroll
                 for (int b = 0; b < kGruGroup; ++b) {
                     if (b < ng) {
-                        const float si = warp_sum(gi[b]), shh = warp_sum(gh[b]);
+                        const float gi = warp_sum(row_dot_smem(wi, sx + b * E, E, lane));
+                        float gh = 0.f;
+                        if (need_gh) gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
+                        else if (u > 0) gh = sgh[((g0 + b) * 64 + jj) * 3 + gate];
                         if (lane == 0) {
-                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 0] = si;
-                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 1] = shh;
+                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 0] = gi;
+                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 1] = gh;
                         }
                     }
                 }
@@ -337,37 +403,26 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         }
     };
 
-    // ---- projector layer 1 + SiLU for step k; writes a
+    // ---- projector layer 1 + SiLU for step k; writes a.  Leaves h_k staged
+    // in sh (single group) for the hidden-side GRU products.
     auto fc1 = [&](int k) {
         const float* hv = p.h + (size_t)h_slot(k) * p.max_B * G;
         for (int g0 = 0; g0 < B; g0 += kGruGroup) {
             const int ng = min(kGruGroup, B - g0);
+            RegRow<T, NCH> w;
+            int f = f0 + warp;
+            if (f < f1) w.load(p.fc1 + (size_t)f * G, G, lane, pol_keep);
             for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
                 const int b = i / G, e = i % G;
                 sh[b * G + e] = __ldcg(&hv[(size_t)(g0 + b) * G + e]);
             }
             cons_sync();
-            for (int f = f0 + warp; f < f1; f += kConsumerWarps) {
-                const T* w = p.fc1 + (size_t)f * G;
-                float acc[kGruGroup];
-#pragma unroll
-                for (int b = 0; b < kGruGroup; ++b) acc[b] = 0.f;
-                for (int e = lane * 8; e < G; e += 256) {
-                    float ww[8];
-                    load8(w + e, ww);
-#pragma unroll
-                    for (int b = 0; b < kGruGroup; ++b)
-                        if (b < ng) {
-                            float x[8];
-                            lds8(sh + b * G + e, x);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) acc[b] = fmaf(ww[q], x[q], acc[b]);
-                        }
-                }
+            for (; f < f1; f += kConsumerWarps) {
+                if (f != f0 + warp) w.load(p.fc1 + (size_t)f * G, G, lane, pol_keep);
 #pragma unroll
                 for (int b = 0; b < kGruGroup; ++b) {
                     if (b < ng) {
-                        float z = warp_sum(acc[b]);
+                        float z = warp_sum(row_dot_smem(w, sh + b * G, G, lane));
                         if (lane == 0) {
                             z += to_f32(p.s[((size_t)(g0 + b) * kProposals + k) * F + f]);
                             p.a[(size_t)(g0 + b) * F + f] = z * sigmoidf_(z);
@@ -390,6 +445,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         }
         cp_async_wait_all();
         cons_sync();
+        float areg[NCH][8];
+        int areg_b = -1;
         unsigned long long best = 0ull;
         int cur = -1;
         const bool fwd = (k & 1) != 0;
@@ -400,49 +457,45 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             const int r = c * kRowsPerSlot + warp;
             if (r < nw) {
                 const T* wrow = reinterpret_cast<const T*>(ring + (size_t)slot * p.slot_bytes + (size_t)warp * row_bytes);
-                if (full_vocab) {
-                    const int v = (int)(w0 + r);
-                    for (int b = 0; b < B; ++b) {
-                        float acc = 0.f;
-                        for (int f = lane * 8; f < F; f += 256) {
-                            float w[8], x[8];
-                            lds8(wrow + f, w);
-                            lds8(sa + b * F + f, x);
+                const long long item = w0 + r;
+                const int bl = full_vocab ? 0 : (int)(item / p.K) - b_first;
+                if (bl != areg_b) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
-                        }
-                        acc = warp_sum(acc);
-                        if (lane == 0) {
-                            const float cv = acc + sbias[r] + sL[b * p.seg + r];
-                            const unsigned long long key = pack_key(cv, (uint32_t)v);
-                            if (B == 1) best = key > best ? key : best;
-                            else atomicMax(&sbest[b], key);
-                            if (p.dbg_scores) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
+                    for (int cc = 0; cc < NCH; ++cc) {
+                        const int e = (lane + 32 * cc) * 8;
+                        if (e < F) lds8(sa + bl * F + e, areg[cc]);
+                    }
+                    areg_b = bl;
+                }
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < NCH; ++cc) {
+                    const int e = (lane + 32 * cc) * 8;
+                    if (e < F) {
+                        float w[8];
+                        lds8(wrow + e, w);
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) {
+                            a0 = fmaf(w[i], areg[cc][i], a0);
+                            a1 = fmaf(w[i + 1], areg[cc][i + 1], a1);
                         }
                     }
-                } else {
-                    const long long item = w0 + r;
-                    const int b = (int)(item / p.K), i = (int)(item % p.K);
-                    const int bl = b - b_first;
-                    float acc = 0.f;
-                    for (int f = lane * 8; f < F; f += 256) {
-                        float w[8], x[8];
-                        lds8(wrow + f, w);
-                        lds8(sa + bl * F + f, x);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
+                }
+                const float acc = warp_sum(a0 + a1);
+                if (lane == 0) {
+                    const int v = full_vocab ? (int)item : p.pool[item];
+                    const float cv = acc + sbias[r] + sL[r];
+                    const unsigned long long key = pack_key(cv, (uint32_t)v);
+                    if (bl != cur) {
+                        if (cur >= 0 && best) atomicMax(&sbest[cur], best);
+                        cur = bl;
+                        best = 0ull;
                     }
-                    acc = warp_sum(acc);
-                    if (lane == 0) {
-                        const float cv = acc + sbias[r] + sL[r];
-                        const unsigned long long key = pack_key(cv, (uint32_t)p.pool[item]);
-                        if (bl != cur) {
-                            if (cur >= 0 && best) atomicMax(&sbest[cur], best);
-                            cur = bl;
-                            best = 0ull;
-                        }
-                        best = key > best ? key : best;
-                        if (p.dbg_scores) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + i] = cv;
+                    best = key > best ? key : best;
+                    if (p.dbg_scores) {
+                        const int b = b_first + bl;
+                        if (full_vocab) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
+                        else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
                     }
                 }
             }
@@ -451,7 +504,22 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             ++q;
             if (tid == 0) *consumed_ptr = q;
         }
-        if (lane == 0 && best) atomicMax(&sbest[full_vocab ? 0 : cur], best);
+        if (lane == 0 && best) atomicMax(&sbest[cur], best);
+        // hidden-side GRU products for the next update while the ring refills
+        if (pre_gh && k < kCorrected && !*abort_flag) {
+            for (int it = warp; it < jn * 3; it += kConsumerWarps) {
+                const int jj = it / 3, gate = it % 3;
+                RegRow<T, NCH> wh;
+                wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
+#pragma unroll
+                for (int b = 0; b < kGruGroup; ++b) {
+                    if (b < B) {
+                        const float gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
+                        if (lane == 0) sgh[(b * 64 + jj) * 3 + gate] = gh;
+                    }
+                }
+            }
+        }
         cons_sync();
         if (tid < b_count) {
             if (sbest[tid]) atomicMax(&p.keys[(size_t)(b_first + tid) * kBlock + k], sbest[tid]);
@@ -461,24 +529,18 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
 
     // base-logit values of step k for the slice, fetched asynchronously
     auto prefetch_L = [&](int k) {
-        if (full_vocab) {
-            for (int i = tid; i < B * nw; i += kConsumerWarps * 32) {
-                const int b = i / nw, r = i % nw;
-                cp_async4(&sL[b * p.seg + r], p.L + ((size_t)b * kBlock + kRowOffset + k) * V + w0 + r);
-            }
-        } else {
-            for (int r = tid; r < nw; r += kConsumerWarps * 32) {
-                const long long item = w0 + r;
-                const int b = (int)(item / p.K);
-                cp_async4(&sL[r], p.L + ((size_t)b * kBlock + kRowOffset + k) * V + p.pool[item]);
-            }
+        for (int r = tid; r < nw; r += kConsumerWarps * 32) {
+            const long long item = w0 + r;
+            const int b = full_vocab ? 0 : (int)(item / p.K);
+            const int v = full_vocab ? (int)item : p.pool[item];
+            cp_async4(&sL[r], p.L + ((size_t)b * kBlock + kRowOffset + k) * V + v);
         }
         cp_async_commit();
     };
 
-    gru(0);
+    gru(0, false);
     if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
-    gru(1);
+    gru(1, false);
     if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
     for (int k = 1; k <= kCorrected; ++k) {
         prefetch_L(k);
@@ -487,7 +549,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         correct(k);
         if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
         if (k < kCorrected) {
-            gru(k + 1);
+            gru(k + 1, pre_gh);
             if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
         }
     }
@@ -515,6 +577,24 @@ Plan make_plan(const domino_ctx* c, int B, int K) {
     Plan pl{seg, slot_bytes, n_slots, 0};
     if (n_slots >= 2) pl.smem = Layout(n_slots, slot_bytes, g.E, g.G, g.F, seg, B, K).total;
     return pl;
+}
+
+// Register-row widths compiled per dtype (bf16 up to rows of 2048; fp32,
+// used by the small fp32 workloads, up to rows of 512).
+template <typename T>
+void (*pick_kernel(int nch))(PersistParams<T>);
+template <>
+void (*pick_kernel<__nv_bfloat16>(int nch))(PersistParams<__nv_bfloat16>) {
+    using T = __nv_bfloat16;
+    return nch <= 1 ? k_rollout_persist<T, 1>
+         : nch <= 2 ? k_rollout_persist<T, 2>
+         : nch <= 4 ? k_rollout_persist<T, 4>
+         : nch <= 6 ? k_rollout_persist<T, 6>
+         : nch <= 8 ? k_rollout_persist<T, 8> : nullptr;
+}
+template <>
+void (*pick_kernel<float>(int nch))(PersistParams<float>) {
+    return nch <= 1 ? k_rollout_persist<float, 1> : nch <= 2 ? k_rollout_persist<float, 2> : nullptr;
 }
 
 template <typename T>
@@ -560,7 +640,10 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     p.n_slots = n_slots;
     p.slot_bytes = slot_bytes;
 
-    auto kern = k_rollout_persist<T>;
+    const int mx = g.E > g.G ? (g.E > g.F ? g.E : g.F) : (g.G > g.F ? g.G : g.F);
+    const int nch = (mx + 255) / 256;
+    void (*kern)(PersistParams<T>) = pick_kernel<T>(nch);
+    if (!kern) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -586,7 +669,9 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
 bool persist_supported(const domino_ctx* c, const RunArgs& r) {
     const domino_config& g = c->cfg;
     const int esize = g.dtype == DOMINO_DTYPE_BF16 ? 2 : 4;
-    if (((g.E | g.G | g.F) & 7) || (g.F * esize) % 16 != 0 || g.F > 2048 || g.E > 2048 || g.G > 2048) return false;
+    const int max_row = esize == 2 ? 2048 : 512;
+    if (((g.E | g.G | g.F) & 7) || (g.F * esize) % 16 != 0 || g.F > max_row || g.E > max_row || g.G > max_row)
+        return false;
     if ((g.G + c->num_sms - 1) / c->num_sms > 64) return false;
     if (r.B > 256) return false;
     const int grid = c->num_sms;

@@ -1,0 +1,223 @@
+// Block-shared candidate pool (page "Add correctness-first Domino support to
+// DFlash V2", section "Design": one per-request pool shared by all steps of
+// the block; page "support tensor-parallel Domino rollout", section
+// "Implementation", stage B): the K token ids with the largest
+//   score[b, v] = max_{i=1..15} L[b, i, v],
+// ties at the cutoff to the lower id, stored in ascending id order.
+//
+// One thread-block cluster of kRanks CTAs per request.  Each CTA caches its
+// contiguous slice of the vocabulary as 32-bit orderable keys in shared
+// memory.  An exact radix select over three digit passes (11, 11, 10 bits)
+// finds the K-th largest key T: each pass builds per-CTA histograms with
+// warp-aggregated shared-memory atomics, merges them through distributed
+// shared memory, and locates the digit holding the K-th key.  The ids with
+// key > T and the lowest-id `need` ids with key == T are then written, each
+// CTA at the offset given by the counts of the CTAs before it, so the pool
+// comes out in ascending order without a sort.
+#include <cooperative_groups.h>
+
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace domino {
+
+namespace {
+
+constexpr int kRanks = 8;          // CTAs per request (portable cluster size)
+constexpr int kPoolThreads = 1024;
+constexpr int kBins = 2048;
+
+struct PoolShared {
+    unsigned hist[kBins];
+    unsigned merged[kBins / kRanks];
+    unsigned warp_tot[32];
+    unsigned total;          // this CTA's merged-bin total / block scan total
+    unsigned gt, eq;         // compaction counts of this CTA
+    unsigned digit, rem;     // result of a pass, written by the CTA that found it
+};
+
+__device__ __forceinline__ unsigned block_scan_excl(unsigned x, unsigned* warp_tot, unsigned* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned t = warp_tot[lane];
+        unsigned ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += y;
+        }
+        warp_tot[lane] = ti - t;
+        if (lane == 31) *total = ti;
+    }
+    __syncthreads();
+    const unsigned r = warp_tot[warp] + incl - x;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* __restrict__ score,
+                                                                 int32_t* __restrict__ pool, int V, int K,
+                                                                 int chunk) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    PoolShared& S = *reinterpret_cast<PoolShared*>(smem);
+    unsigned* keys = reinterpret_cast<unsigned*>(smem + sizeof(PoolShared));
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int v0 = min(V, rank * chunk), v1 = min(V, v0 + chunk), n = v1 - v0;
+
+    const float* sc = score + (size_t)b * V + v0;
+    for (int i = threadIdx.x; i < n; i += kPoolThreads) keys[i] = ord_f32(sc[i]);
+
+    unsigned prefix = 0, pmask = 0, remaining = (unsigned)K;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = shifts[pass];
+        const unsigned nb = 1u << widths[pass];
+        const unsigned dmask = nb - 1;
+        for (unsigned i = threadIdx.x; i < nb; i += kPoolThreads) S.hist[i] = 0;
+        __syncthreads();
+        const int n_round = (n + 31) & ~31;
+        for (int i = threadIdx.x; i < n_round; i += kPoolThreads) {
+            const unsigned k = i < n ? keys[i] : 0u;
+            const bool part = i < n && (k & pmask) == prefix;
+            const unsigned m = __ballot_sync(0xffffffffu, part);
+            if (part) {
+                const unsigned d = (k >> shift) & dmask;
+                const unsigned peers = __match_any_sync(m, d);
+                if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[d], (unsigned)__popc(peers));
+            }
+        }
+        cluster.sync();  // every CTA's histogram is complete
+        // this CTA merges the bins [rank*per, (rank+1)*per) of all CTAs
+        const unsigned per = nb / kRanks;
+        unsigned mine = 0;
+        for (unsigned t = threadIdx.x; t < per; t += kPoolThreads) {
+            unsigned s = 0;
+#pragma unroll
+            for (int r = 0; r < kRanks; ++r) s += cluster.map_shared_rank(S.hist, r)[rank * per + t];
+            S.merged[t] = s;
+            mine += s;
+        }
+        // block total of the merged slice
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+        if (lane == 0) S.warp_tot[threadIdx.x >> 5] = mine;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned t = 0;
+            for (int w = 0; w < kPoolThreads / 32; ++w) t += S.warp_tot[w];
+            S.total = t;
+        }
+        cluster.sync();  // merged slices and their totals are visible
+        // the K-th largest key lies in the highest slice whose suffix reaches `remaining`
+        if (threadIdx.x == 0) {
+            unsigned cum = 0;
+            int R = 0;
+            for (int r = kRanks - 1; r >= 0; --r) {
+                const unsigned t = *cluster.map_shared_rank(&S.total, r);
+                if (cum + t >= remaining) {
+                    R = r;
+                    break;
+                }
+                cum += t;
+            }
+            const unsigned* mg = cluster.map_shared_rank(S.merged, R);
+            unsigned rem = remaining - cum;
+            int d = (int)per - 1;
+            for (; d > 0; --d) {
+                const unsigned h = mg[d];
+                if (h >= rem) break;
+                rem -= h;
+            }
+            S.digit = (unsigned)R * per + (unsigned)d;
+            S.rem = rem;
+        }
+        cluster.sync();  // remote reads done before the histograms are reused
+        prefix |= S.digit << shift;
+        pmask |= dmask << shift;
+        remaining = S.rem;
+    }
+    const unsigned T = prefix, need = remaining;  // take `need` of the ids whose key equals T
+
+    // ordered compaction: each thread owns a contiguous run of this CTA's slice
+    const int per_t = (n + kPoolThreads - 1) / kPoolThreads;
+    const int i0 = min(n, (int)threadIdx.x * per_t), i1 = min(n, i0 + per_t);
+    unsigned gt = 0, eq = 0;
+    for (int i = i0; i < i1; ++i) {
+        gt += keys[i] > T;
+        eq += keys[i] == T;
+    }
+    const unsigned eq_before_t = block_scan_excl(eq, S.warp_tot, &S.total);
+    const unsigned eq_cta = S.total;
+    const unsigned gt_before_t = block_scan_excl(gt, S.warp_tot, &S.total);
+    const unsigned gt_cta = S.total;
+    if (threadIdx.x == 0) {
+        S.gt = gt_cta;
+        S.eq = eq_cta;
+    }
+    cluster.sync();
+    unsigned gt_before_r = 0, eq_before_r = 0;
+    for (int r = 0; r < rank; ++r) {
+        gt_before_r += *cluster.map_shared_rank(&S.gt, r);
+        eq_before_r += *cluster.map_shared_rank(&S.eq, r);
+    }
+    const unsigned eq_before = eq_before_r + eq_before_t;
+    const unsigned eq_take = eq_before >= need ? 0u : min(eq, need - eq_before);
+    // ids written before this thread: all greater ones, and the equal ones taken so far
+    unsigned pos = gt_before_r + gt_before_t + min(need, eq_before);
+    int32_t* out = pool + (size_t)b * K;
+    unsigned eq_used = 0;
+    for (int i = i0; i < i1; ++i) {
+        const unsigned k = keys[i];
+        bool take = k > T;
+        if (!take && k == T && eq_used < eq_take) {
+            take = true;
+            ++eq_used;
+        }
+        if (take && pos < (unsigned)K) out[pos++] = v0 + i;
+    }
+    cluster.sync();  // no CTA leaves while others may still read its shared memory
+}
+
+}  // namespace
+
+bool pool_cluster_supported(const domino_ctx* c) {
+    const int chunk = (c->cfg.V + kRanks - 1) / kRanks;
+    return sizeof(PoolShared) + (size_t)chunk * 4 <= 220 * 1024;
+}
+
+cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r) {
+    const int chunk = (c->cfg.V + kRanks - 1) / kRanks;
+    const size_t smem = sizeof(PoolShared) + (size_t)chunk * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_pool_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kRanks, r.B);
+    cfg.blockDim = dim3(kPoolThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = r.st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kRanks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_pool_cluster, (const float*)c->score, c->pool, c->cfg.V, r.K, chunk);
+    ++r.launches;
+    return e;
+}
+
+}  // namespace domino

@@ -203,3 +203,30 @@ def test_batch_independence():
             single = eng.run(*device_requests(one), K=K).cpu().numpy()
             assert (single[0] == whole[b]).all(), (K, b)
         eng.close()
+
+
+@pytest.mark.parametrize("K", [1, 50, 300, 600])
+def test_pool_cutoff_inside_a_large_tie_group(K):
+    """Hundreds of vocabulary rows share one LM-head row, so the pool cutoff
+    falls inside a group of exactly equal scores: the lowest ids must win."""
+    sh = inputs.small_shape(V=2000, dtype="bf16")
+    sc = FEEDBACK_SCALES(sh)
+    w = {k: v.copy() for k, v in cached_weights(sh, 0, sc).items()}
+    r = inputs.make_requests(sh, [5, 6])
+    # make row 1234 score high, then clone it over 600 scattered ids
+    w["lm_head"][1234] = inputs.to_bf16_bits((oracle.widen(w["lm_head"][1234]) * 6.0).astype(np.float32))
+    ids = np.random.default_rng(3).choice(sh.V, size=600, replace=False)
+    for v in ids:
+        w["lm_head"][v] = w["lm_head"][1234]
+    ow = oracle.OracleWeights(w)
+    o = oracle.rollout(ow, r["hidden"], r["s"], r["verified"], K)
+    score = o["L"][:, 1:16].max(axis=1)
+    for b in range(2):  # the cutoff really sits inside the tie group
+        kth = np.sort(score[b])[::-1][K - 1]
+        assert (score[b] == kth).sum() > 1
+    eng = make_engine(sh, max_B=2, max_K=K, dw=device_weights(w))
+    g = gpu_debug(eng, sh, device_requests(r), 2, K, o["tokens"])
+    for b in range(2):
+        assert g["pool"][b].tolist() == o["pool"][b].tolist()
+    check_against_oracle(ow, o, g, sh, K)
+    eng.close()
