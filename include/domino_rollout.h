@@ -113,7 +113,12 @@ typedef struct {
     float*   z;       /* [B,14,F] projector pre-activation of each step         */
     float*   top1;    /* [B,15] winning score of each proposal                  */
     float*   scores;  /* [B,14,Kc] corrected scores, Kc = V (K0) or K (pool)    */
+    unsigned long long* trace; /* [grid,DOMINO_TRACE_SLOTS] %globaltimer stamps (ns)
+                                  of the persistent driver's phase boundaries per
+                                  CTA (grid = SM count); untouched by the other
+                                  driver */
 } domino_debug_bufs;
+#define DOMINO_TRACE_SLOTS 96
 
 /* As domino_rollout_run, plus teacher forcing and dumps.  forced_tokens
  * (nullable DEVICE [B,15] int32): when given, the GRU is fed forced[b,k]

@@ -35,7 +35,11 @@ namespace {
 // 15 consumer warps + 1 producer warp: 16 warps leave 128 registers a thread
 constexpr int kConsumerWarps = 15;
 constexpr int kPersistThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRowsPerSlot = kConsumerWarps;  // one row per consumer warp per slot
+constexpr int kRowsPerSlot = 4;    // rows per ring slot; one warp consumes a whole slot
+constexpr int kMaxSlots = 48;
+// Ring slot q % n_slots is consumed by warp q % n_cons alone (n_cons divides
+// n_slots): each slot has one waiting consumer and the producer, so a parity
+// wait can never observe a fill that belongs to a later pass over the ring.
 constexpr int kMaxReq = 8;         // requests a CTA may touch in phase C
 constexpr int kGruGroup = 4;       // requests per GRU/fc1 staging group
 constexpr int kMaxSeg = 2048;      // rows (or pool entries) per CTA
@@ -51,9 +55,11 @@ struct PersistParams {
     int *bad, *err;
     unsigned int* sync;
     float *dbg_h, *dbg_z, *dbg_scores;
+    unsigned long long* trace;  // [grid][DOMINO_TRACE_SLOTS] or null
     int B, K, V, E, G, F, max_B;
     int seg;        // rows (K0) or pool entries per CTA
     int n_slots;
+    int n_cons;     // consumer warps of the correction phase (divides n_slots)
     int slot_bytes;
 };
 
@@ -180,6 +186,82 @@ __device__ __forceinline__ float row_dot_smem(const RegRow<T, NCH>& w, const flo
     return a0 + a1;
 }
 
+// Two independent fp32 FMAs in one instruction (round to nearest, like fmaf).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long A, Bv, C, D;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(Bv) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(Bv), "l"(C));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(D));
+    return d;
+}
+// 8 elements of a shared-memory row as 4 (even, odd) pairs
+__device__ __forceinline__ void lds_pairs(const __nv_bfloat16* p, float2* o) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    o[0] = make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u));
+    o[1] = make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+    o[2] = make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u));
+    o[3] = make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
+}
+__device__ __forceinline__ void lds_pairs(const float* p, float2* o) {
+    const float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
+    o[0] = make_float2(x.x, x.y);
+    o[1] = make_float2(x.z, x.w);
+    o[2] = make_float2(y.x, y.y);
+    o[3] = make_float2(y.z, y.w);
+}
+
+// 16-byte chunk of 8 row elements held in registers
+template <typename T>
+struct ChunkOf;
+template <>
+struct ChunkOf<__nv_bfloat16> {
+    using type = uint4;
+    __device__ __forceinline__ static uint4 load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
+    __device__ __forceinline__ static void pairs(const uint4& q, float2* o) {
+        o[0] = make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u));
+        o[1] = make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+        o[2] = make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u));
+        o[3] = make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
+    }
+};
+struct F8 {
+    float4 a, b;
+};
+template <>
+struct ChunkOf<float> {
+    using type = F8;
+    __device__ __forceinline__ static F8 load(const float* p) {
+        return F8{reinterpret_cast<const float4*>(p)[0], reinterpret_cast<const float4*>(p)[1]};
+    }
+    __device__ __forceinline__ static void pairs(const F8& q, float2* o) {
+        o[0] = make_float2(q.a.x, q.a.y);
+        o[1] = make_float2(q.a.z, q.a.w);
+        o[2] = make_float2(q.b.x, q.b.y);
+        o[3] = make_float2(q.b.z, q.b.w);
+    }
+};
+
+// Sum each of 4 per-lane values over the warp with 6 shuffles (a transposed
+// butterfly).  Lane l ends with the total of value ((l >> 4) & 1) * 2 +
+// ((l >> 3) & 1).
+__device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v3, int lane) {
+    const bool hi16 = (lane & 16) != 0;
+    float a = hi16 ? v2 : v0, b = hi16 ? v3 : v1;          // keep
+    float c = hi16 ? v0 : v2, d = hi16 ? v1 : v3;          // send
+    a += __shfl_xor_sync(0xffffffffu, c, 16);
+    b += __shfl_xor_sync(0xffffffffu, d, 16);
+    const bool hi8 = (lane & 8) != 0;
+    float keep = hi8 ? b : a, send = hi8 ? a : b;
+    keep += __shfl_xor_sync(0xffffffffu, send, 8);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+    return keep;
+}
+
 // Shared-memory layout (bytes, all offsets 128-aligned)
 // Requests whose activations one CTA needs in phase C.
 __host__ __device__ inline int phase_c_requests(int B, int K, int seg) {
@@ -244,7 +326,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     if (tid == 0) {
         for (int s = 0; s < p.n_slots; ++s) {
             tc::mbar_init(full0 + 8 * s, 1);
-            tc::mbar_init(empty0 + 8 * s, kConsumerWarps);
+            tc::mbar_init(empty0 + 8 * s, 1);
         }
         *abort_flag = 0;
         *consumed_ptr = 0;
@@ -289,8 +371,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             const unsigned long long t0 = tc::globaltimer();
             while (*consumed_ptr < q && !*abort_flag && tc::globaltimer() - t0 < tc::kWaitLimitNs) {
             }
-            if (*consumed_ptr < q) {
-                for (int i = *consumed_ptr; i < q; ++i) {
+            if (*consumed_ptr < q) {  // aborted: the last ring-full of copies may still be landing
+                for (int i = q > p.n_slots ? q - p.n_slots : 0; i < q; ++i) {
                     const int s = i % p.n_slots;
                     const unsigned long long t1 = tc::globaltimer();
                     while (!tc::mbar_try_wait(full0 + 8 * s, (uint32_t)((i / p.n_slots) & 1)) &&
@@ -435,8 +517,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         }
     };
 
-    // ---- correction + argmax of step k over this CTA's slice
-    int q = 0;  // ring position, in step with the producer
+    // ---- correction + argmax of step k over this CTA's slice.  Ring slot q
+    // (kRowsPerSlot rows) is consumed by warp q % n_cons alone.
     auto correct = [&](int k) {
         // activations of the requests this slice touches
         for (int i = tid; i < b_count * F; i += kConsumerWarps * 32) {
@@ -447,64 +529,117 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         cons_sync();
         float areg[NCH][8];
         int areg_b = -1;
-        unsigned long long best = 0ull;
+        unsigned long long best = 0ull;  // running best of the rows this lane finalises
         int cur = -1;
         const bool fwd = (k & 1) != 0;
-        for (int ci = 0; ci < n_chunks; ++ci) {
+        const int qb = (k - 1) * n_chunks;
+        const int nc = p.n_cons;
+        int q = warp < nc ? qb + ((warp - qb) % nc + nc) % nc : qb + n_chunks;
+        for (; q < qb + n_chunks; q += nc) {
+            const int ci = q - qb;
             const int c = fwd ? ci : n_chunks - 1 - ci;
             const int slot = q % p.n_slots;
             if (!tc::mbar_wait(full0 + 8 * slot, (uint32_t)((q / p.n_slots) & 1), abort_flag, p.err)) break;
-            const int r = c * kRowsPerSlot + warp;
-            if (r < nw) {
-                const T* wrow = reinterpret_cast<const T*>(ring + (size_t)slot * p.slot_bytes + (size_t)warp * row_bytes);
-                const long long item = w0 + r;
-                const int bl = full_vocab ? 0 : (int)(item / p.K) - b_first;
-                if (bl != areg_b) {
+            const int r0 = c * kRowsPerSlot;
+            const int nr = min(kRowsPerSlot, nw - r0);
+            // requests of the slot's first and last rows (a slot spans two only
+            // at a request boundary of the pool)
+            const int bl0 = full_vocab ? 0 : (int)((w0 + r0) / p.K) - b_first;
+            const int bl1 = full_vocab ? 0 : (int)((w0 + r0 + nr - 1) / p.K) - b_first;
+            const T* srow = reinterpret_cast<const T*>(ring + (size_t)slot * p.slot_bytes);
+            float part[kRowsPerSlot];
+            if (bl0 == bl1) {
+                if (bl0 != areg_b) {  // warp-uniform; once per step (full vocabulary)
 #pragma unroll
                     for (int cc = 0; cc < NCH; ++cc) {
                         const int e = (lane + 32 * cc) * 8;
-                        if (e < F) lds8(sa + bl * F + e, areg[cc]);
+                        if (e < F) lds8(sa + bl0 * F + e, areg[cc]);
                     }
-                    areg_b = bl;
+                    areg_b = bl0;
                 }
-                float a0 = 0.f, a1 = 0.f;
+                // the slot's rows as independent FMA chains
+                float acc[kRowsPerSlot][2];
+#pragma unroll
+                for (int rr = 0; rr < kRowsPerSlot; ++rr) acc[rr][0] = acc[rr][1] = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < NCH; ++cc) {
                     const int e = (lane + 32 * cc) * 8;
                     if (e < F) {
-                        float w[8];
-                        lds8(wrow + e, w);
 #pragma unroll
-                        for (int i = 0; i < 8; i += 2) {
-                            a0 = fmaf(w[i], areg[cc][i], a0);
-                            a1 = fmaf(w[i + 1], areg[cc][i + 1], a1);
+                        for (int rr = 0; rr < kRowsPerSlot; ++rr) {
+                            if (rr < nr) {
+                                float w[8];
+                                lds8(srow + (size_t)rr * F + e, w);
+#pragma unroll
+                                for (int i = 0; i < 8; i += 2) {
+                                    acc[rr][0] = fmaf(w[i], areg[cc][i], acc[rr][0]);
+                                    acc[rr][1] = fmaf(w[i + 1], areg[cc][i + 1], acc[rr][1]);
+                                }
+                            }
                         }
                     }
                 }
-                const float acc = warp_sum(a0 + a1);
-                if (lane == 0) {
-                    const int v = full_vocab ? (int)item : p.pool[item];
-                    const float cv = acc + sbias[r] + sL[r];
-                    const unsigned long long key = pack_key(cv, (uint32_t)v);
-                    if (bl != cur) {
-                        if (cur >= 0 && best) atomicMax(&sbest[cur], best);
-                        cur = bl;
-                        best = 0ull;
-                    }
-                    best = key > best ? key : best;
-                    if (p.dbg_scores) {
-                        const int b = b_first + bl;
-                        if (full_vocab) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
-                        else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
+#pragma unroll
+                for (int rr = 0; rr < kRowsPerSlot; ++rr) part[rr] = acc[rr][0] + acc[rr][1];
+            } else {
+                // rows of two requests: one row at a time with its own activations
+#pragma unroll
+                for (int rr = 0; rr < kRowsPerSlot; ++rr) {
+                    part[rr] = 0.f;
+                    if (rr < nr) {
+                        const int bl = (int)((w0 + r0 + rr) / p.K) - b_first;
+                        if (bl != areg_b) {
+#pragma unroll
+                            for (int cc = 0; cc < NCH; ++cc) {
+                                const int e = (lane + 32 * cc) * 8;
+                                if (e < F) lds8(sa + bl * F + e, areg[cc]);
+                            }
+                            areg_b = bl;
+                        }
+                        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                        for (int cc = 0; cc < NCH; ++cc) {
+                            const int e = (lane + 32 * cc) * 8;
+                            if (e < F) {
+                                float w[8];
+                                lds8(srow + (size_t)rr * F + e, w);
+#pragma unroll
+                                for (int i = 0; i < 8; i += 2) {
+                                    a0 = fmaf(w[i], areg[cc][i], a0);
+                                    a1 = fmaf(w[i + 1], areg[cc][i + 1], a1);
+                                }
+                            }
+                        }
+                        part[rr] = a0 + a1;
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
-            ++q;
-            if (tid == 0) *consumed_ptr = q;
+            if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);  // the slot is read: hand it back
+            const float tot = warp_sum4(part[0], part[1], part[2], part[3], lane);
+            const int rsel = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            if ((lane & 7) == 0 && rsel < nr) {  // four lanes finish four rows
+                const int r = r0 + rsel;
+                const long long item = w0 + r;
+                const int bl = full_vocab ? 0 : (int)(item / p.K) - b_first;
+                const int v = full_vocab ? (int)item : p.pool[item];
+                const float cv = tot + sbias[r] + sL[r];
+                const unsigned long long key = pack_key(cv, (uint32_t)v);
+                if (bl != cur) {
+                    if (cur >= 0 && best) atomicMax(&sbest[cur], best);
+                    cur = bl;
+                    best = 0ull;
+                }
+                best = key > best ? key : best;
+                if (p.dbg_scores) {
+                    const int b = b_first + bl;
+                    if (full_vocab) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
+                    else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
+                }
+            }
+            if (lane == 0) atomicAdd((int*)consumed_ptr, 1);
         }
-        if (lane == 0 && best) atomicMax(&sbest[cur], best);
+        if (best) atomicMax(&sbest[cur], best);
         // hidden-side GRU products for the next update while the ring refills
         if (pre_gh && k < kCorrected && !*abort_flag) {
             for (int it = warp; it < jn * 3; it += kConsumerWarps) {
@@ -538,25 +673,46 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         cp_async_commit();
     };
 
-    gru(0, false);
-    if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
-    gru(1, false);
-    if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
-    for (int k = 1; k <= kCorrected; ++k) {
-        prefetch_L(k);
-        fc1(k);
+    // optional trace: stamp s of this CTA = time at the end of phase s
+    unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * DOMINO_TRACE_SLOTS : nullptr;
+    int ts = 0;
+    auto stamp = [&]() {
+        if (tr && tid == 0 && ts < DOMINO_TRACE_SLOTS) tr[ts] = tc::globaltimer();
+        ++ts;
+    };
+    auto body = [&]() {
+        stamp();                                                     // 0: start
+        gru(0, false);
+        stamp();                                                     // 1
         if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
-        correct(k);
+        stamp();                                                     // 2
+        gru(1, false);
+        stamp();                                                     // 3
         if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
-        if (k < kCorrected) {
-            gru(k + 1, pre_gh);
+        stamp();                                                     // 4
+        for (int k = 1; k <= kCorrected; ++k) {                      // 5 + 6 (k-1) + ...
+            prefetch_L(k);
+            fc1(k);
+            stamp();                                                 // +0 projector done
             if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+            stamp();                                                 // +1 barrier
+            correct(k);
+            stamp();                                                 // +2 correction done
+            if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+            stamp();                                                 // +3 barrier
+            if (k < kCorrected) {
+                gru(k + 1, pre_gh);
+                stamp();                                             // +4 GRU done
+                if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+                stamp();                                             // +5 barrier
+            }
         }
-    }
+    };
+    body();
 }
 
 struct Plan {
-    int seg, slot_bytes, n_slots, smem;
+    int seg, slot_bytes, n_slots, n_cons, smem;
 };
 
 // Per-CTA slice, ring slot size and ring depth: the ring gets what the rest
@@ -573,8 +729,17 @@ Plan make_plan(const domino_ctx* c, int B, int K) {
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     Layout base(0, slot_bytes, g.E, g.G, g.F, seg, B, K);
     int n_slots = (max_smem - base.total - 1024) / (slot_bytes + 16);
-    if (n_slots > 12) n_slots = 12;
-    Plan pl{seg, slot_bytes, n_slots, 0};
+    if (n_slots > kMaxSlots) n_slots = kMaxSlots;
+    // consumer warps: the count (<= kConsumerWarps) whose multiple uses the most slots
+    int n_cons = n_slots < kConsumerWarps ? n_slots : kConsumerWarps;
+    int best = n_cons > 0 ? n_slots / n_cons * n_cons : 0;
+    for (int w = n_cons - 1; w >= 8; --w)
+        if (n_slots / w * w > best) {
+            best = n_slots / w * w;
+            n_cons = w;
+        }
+    Plan pl{seg, slot_bytes, best, n_cons, 0};
+    n_slots = best;
     if (n_slots >= 2) pl.smem = Layout(n_slots, slot_bytes, g.E, g.G, g.F, seg, B, K).total;
     return pl;
 }
@@ -603,7 +768,7 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     const int grid = c->num_sms;
     const Plan pl = make_plan(c, r.B, r.K);
     if (pl.n_slots < 2) return cudaErrorNotSupported;
-    const int seg = pl.seg, slot_bytes = pl.slot_bytes, n_slots = pl.n_slots;
+    const int seg = pl.seg, slot_bytes = pl.slot_bytes, n_slots = pl.n_slots, n_cons = pl.n_cons;
     struct {
         int total;
     } lay{pl.smem};
@@ -629,6 +794,7 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     p.dbg_h = r.dbg.h;
     p.dbg_z = r.dbg.z;
     p.dbg_scores = r.dbg.scores;
+    p.trace = r.dbg.trace;
     p.B = r.B;
     p.K = r.K;
     p.V = g.V;
@@ -638,6 +804,7 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     p.max_B = g.max_B;
     p.seg = seg;
     p.n_slots = n_slots;
+    p.n_cons = n_cons;
     p.slot_bytes = slot_bytes;
 
     const int mx = g.E > g.G ? (g.E > g.F ? g.E : g.F) : (g.G > g.F ? g.G : g.F);

@@ -121,28 +121,48 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
             S.total = t;
         }
         cluster.sync();  // merged slices and their totals are visible
-        // the K-th largest key lies in the highest slice whose suffix reaches `remaining`
-        if (threadIdx.x == 0) {
-            unsigned cum = 0;
-            int R = 0;
-            for (int r = kRanks - 1; r >= 0; --r) {
-                const unsigned t = *cluster.map_shared_rank(&S.total, r);
-                if (cum + t >= remaining) {
-                    R = r;
-                    break;
-                }
-                cum += t;
+        // the K-th largest key lies in the highest slice whose suffix reaches
+        // `remaining`, then in the highest bin of that slice that does: one
+        // warp scans the slice totals and the slice's bins in parallel
+        if (threadIdx.x < 32) {
+            const unsigned t = lane < kRanks ? *cluster.map_shared_rank(&S.total, lane) : 0u;
+            unsigned suf = t;  // inclusive suffix over ranks lane..kRanks-1
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += y;
             }
+            const unsigned hit = __ballot_sync(0xffffffffu, lane < kRanks && suf >= remaining);
+            const int R = 31 - __clz(hit);  // highest rank whose suffix reaches `remaining`
+            const unsigned above = __shfl_sync(0xffffffffu, suf, R) - __shfl_sync(0xffffffffu, t, R);
+            const unsigned rem = remaining - above;
             const unsigned* mg = cluster.map_shared_rank(S.merged, R);
-            unsigned rem = remaining - cum;
-            int d = (int)per - 1;
-            for (; d > 0; --d) {
-                const unsigned h = mg[d];
-                if (h >= rem) break;
-                rem -= h;
+            const int ppl = (int)per / 32;  // bins per lane (8 or 4)
+            unsigned vals[8];
+            unsigned lsum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                vals[i] = i < ppl ? mg[lane * ppl + i] : 0u;
+                lsum += vals[i];
             }
-            S.digit = (unsigned)R * per + (unsigned)d;
-            S.rem = rem;
+            unsigned lsuf = lsum;  // inclusive suffix of lane sums
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_down_sync(0xffffffffu, lsuf, o);
+                if (lane + o < 32) lsuf += y;
+            }
+            unsigned acc = lsuf - lsum;  // keys in the bins of higher lanes
+#pragma unroll
+            for (int i = 7; i >= 0; --i) {
+                if (i < ppl) {
+                    const unsigned before = acc;  // keys in bins above bin (lane*ppl + i)
+                    acc += vals[i];
+                    if (before < rem && acc >= rem) {
+                        S.digit = (unsigned)R * per + (unsigned)(lane * ppl + i);
+                        S.rem = rem - before;
+                    }
+                }
+            }
         }
         cluster.sync();  // remote reads done before the histograms are reused
         prefix |= S.digit << shift;

@@ -104,6 +104,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Bulk prefetch of global bytes into L2 (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+// Prefetch of one tensor-map box into L2.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "l"(policy)
+                 : "memory");
+}
+
 // ---- tcgen05 ---------------------------------------------------------------
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes grouped by 8 (1024-byte swizzle atoms, SBO = 1024).

@@ -49,7 +49,11 @@ class domino_config(ctypes.Structure):
 
 class domino_debug_bufs(ctypes.Structure):
     _fields_ = [("logits", ctypes.c_void_p), ("pool", ctypes.c_void_p), ("h", ctypes.c_void_p),
-                ("z", ctypes.c_void_p), ("top1", ctypes.c_void_p), ("scores", ctypes.c_void_p)]
+                ("z", ctypes.c_void_p), ("top1", ctypes.c_void_p), ("scores", ctypes.c_void_p),
+                ("trace", ctypes.c_void_p)]
+
+
+DOMINO_TRACE_SLOTS = 96
 
 
 class DominoError(RuntimeError):
@@ -135,7 +139,7 @@ def domino_rollout_run(ctx, hidden, s, verified_tok, B: int, K: int, out_tokens,
 
 def domino_rollout_debug_run(ctx, hidden, s, verified_tok, B: int, K: int, forced_tokens, dbg: dict,
                              out_tokens, stream=None) -> int:
-    bufs = domino_debug_bufs(*[_ptr(dbg.get(n)) for n in ("logits", "pool", "h", "z", "top1", "scores")])
+    bufs = domino_debug_bufs(*[_ptr(dbg.get(n)) for n in ("logits", "pool", "h", "z", "top1", "scores", "trace")])
     return load_library().domino_rollout_debug_run(ctx, _ptr(hidden), _ptr(s), _ptr(verified_tok), B, K,
                                                    _ptr(forced_tokens), ctypes.byref(bufs), _ptr(out_tokens),
                                                    _stream(stream))
