@@ -88,7 +88,8 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         if (!persist_supported(c, r)) return DOMINO_ERR_UNSUPPORTED;
         use_persist = true;
     } else if (c->driver == DOMINO_DRIVER_AUTO) {
-        use_persist = persist_supported(c, r);
+        // one request: the persistent driver; batches: the batched kernels
+        use_persist = r.B == 1 && persist_supported(c, r);
     }
 
     cudaError_t e;
@@ -132,6 +133,8 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
             STEP(DOMINO_PHASE_FC1, FC1(k));
             if (tc_corr)
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_tc(c, r, tm_a, k));
+            else if (r.K > 0 && batch && pool_batch_supported(c))
+                STEP(DOMINO_PHASE_CORRECT, launch_correct_pool_batch(c, r, k));
             else
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
             if (k < kCorrected) STEP(DOMINO_PHASE_GRU, GRU(k + 1));

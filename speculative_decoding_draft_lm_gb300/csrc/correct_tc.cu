@@ -31,16 +31,28 @@ struct EpiCorrect {
         for (int b = t; b < n; b += 128)
             if (sb[b]) atomicMax(&keys[(size_t)b * kBlock + k], sb[b]);
     }
+    // base logits of the tile's first PF requests for this thread's row
+    template <int PF>
+    __device__ __forceinline__ void prefetch(int col0, int row, float* pf) const {
+        const bool ok = row < V;
+#pragma unroll
+        for (int j = 0; j < PF; ++j)
+            pf[j] = (ok && col0 + j < B) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
+    }
     __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane,
-                                               unsigned long long* sb) const {
+                                               unsigned long long* sb, const float* pf) const {
         if (col0 >= B) return;  // uniform: padding columns
         const bool ok = row < V;
         const int nb = B - col0 < 16 ? B - col0 : 16;
-        // all base-logit loads of the chunk are in flight before any is used
         float base[16];
+        if (pf) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            base[j] = (ok && j < nb) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
+            for (int j = 0; j < 16; ++j) base[j] = pf[j];
+        } else {  // beyond the prefetch window: all loads of the chunk in flight at once
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                base[j] = (ok && j < nb) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
+        }
         const float bv = ok ? __bfloat162float(bias[row]) : 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {

@@ -9,9 +9,12 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
 //               row of A), handed to the Epi functor 16 columns at a time
 //
-// Epi provides begin(scratch, t) / operator()(col0, row, v[16], lane, scratch)
-// / end(scratch, t), t = epilogue thread 0..127; `scratch` is kEpiScratch
-// per-block 64-bit words (per-request argmax words) in shared memory.
+// Epi provides begin(scratch, t) / prefetch(col0, row, pf) /
+// operator()(col0, row, v[16], lane, scratch, pf + 16c) / end(scratch, t),
+// t = epilogue thread 0..127; `scratch` is kEpiScratch per-block 64-bit words
+// (per-request argmax words) in shared memory; `pf` holds up to kPrefetch
+// values per thread that the epilogue may load for the next tile while the
+// MMAs of that tile are still running.
 //
 // Tiles are visited m-major (tile t -> m = t / n_tiles, n = t % n_tiles), grid
 // stride over a persistent grid of one CTA per SM, so CTAs that share an A
@@ -29,6 +32,7 @@ constexpr int kBM = 128;          // rows of A per tile (MMA M)
 constexpr int kBK = 64;           // K elements per chunk (128 bytes of bf16)
 constexpr int kGemmThreads = 192;
 constexpr int kEpiScratch = 256;  // 64-bit words
+constexpr int kPrefetch = 64;     // per-thread epilogue prefetch registers
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -172,18 +176,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t acc_phase = 0;
         epi.begin(scratch, et);
         epi_bar();
+        constexpr int PF = BN < kPrefetch ? BN : kPrefetch;
+        float pf[PF];
+        if ((int)blockIdx.x < tiles) {
+            const int t0 = blockIdx.x;
+            epi.template prefetch<PF>((t0 % n_tiles) * BN, (t0 / n_tiles) * kBM + quarter * 32 + lane, pf);
+        }
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) break;
             tc_fence_after();
             const int m = t / n_tiles, n = t % n_tiles;
             const int row = m * kBM + quarter * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < BN / 16; ++c) {
                 float v[16];
                 tmem_ld16(tbase + 16 * c, v);
-                epi(n * BN + 16 * c, row, v, lane, scratch);
+                epi(n * BN + 16 * c, row, v, lane, scratch, 16 * c < PF ? pf + 16 * c : nullptr);
             }
+            const int tn = t + gridDim.x;  // the next tile's epilogue inputs, during its MMAs
+            if (tn < tiles)
+                epi.template prefetch<PF>((tn % n_tiles) * BN, (tn / n_tiles) * kBM + quarter * 32 + lane, pf);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
             if (++acc == 2) {

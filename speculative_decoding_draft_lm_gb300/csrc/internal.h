@@ -50,6 +50,8 @@ cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r);
 bool batch_kernels_supported(const domino_ctx* c);
 cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u);
 cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k);
+bool pool_batch_supported(const domino_ctx* c);
+cudaError_t launch_correct_pool_batch(domino_ctx* c, RunArgs& r, int k);
 
 // persistent driver of the GRU seed and the 14 corrected steps (persist.cu)
 bool persist_supported(const domino_ctx* c, const RunArgs& r);

@@ -208,6 +208,141 @@ __global__ void __launch_bounds__(kBatchThreads) k_fc1_batch(const T* __restrict
     }
 }
 
+// Correction + argmax over each request's candidate pool (B >= 2): a warp
+// takes 4 pool entries at a time, requests all 4 gathered fc2 rows before
+// using any (16-byte loads that bypass L1), keeps its request's activations
+// in registers, and finishes the 4 rows on 4 lanes after one transposed warp
+// reduction.  c = fc2[v] . a[b] + bias[v] + L[b, k+1, v], lowest id on ties.
+constexpr int kPoolRows = 4;
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 q;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                 : "l"(p));
+    return q;
+}
+
+// each of 4 per-lane values summed over the warp (6 shuffles); lane l holds
+// the total of value ((l >> 4) & 1) * 2 + ((l >> 3) & 1)
+__device__ __forceinline__ float warp_sum4_t(float v0, float v1, float v2, float v3, int lane) {
+    const bool hi16 = (lane & 16) != 0;
+    float a = hi16 ? v2 : v0, b = hi16 ? v3 : v1;
+    const float c = hi16 ? v0 : v2, d = hi16 ? v1 : v3;
+    a += __shfl_xor_sync(0xffffffffu, c, 16);
+    b += __shfl_xor_sync(0xffffffffu, d, 16);
+    const bool hi8 = (lane & 8) != 0;
+    float keep = hi8 ? b : a;
+    const float send = hi8 ? a : b;
+    keep += __shfl_xor_sync(0xffffffffu, send, 8);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+    return keep;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kBatchThreads) k_correct_pool_batch(
+    const __nv_bfloat16* __restrict__ fc2, const __nv_bfloat16* __restrict__ bias, const float* __restrict__ L,
+    const float* __restrict__ a, const int32_t* __restrict__ pool, unsigned long long* __restrict__ keys,
+    float* __restrict__ dbg_scores, int k, int B, int V, int F, int K, int items_per_block) {
+    __shared__ unsigned long long sbest[64];
+    const long long items = (long long)B * K;
+    const long long i0 = (long long)blockIdx.x * items_per_block;
+    const long long i1 = min(items, i0 + items_per_block);
+    if (i0 >= i1) return;
+    const int b_first = (int)(i0 / K);
+    const int nreq = (int)((i1 - 1) / K) - b_first + 1;  // <= 64 by the launch
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) sbest[i] = 0ull;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = kBatchThreads / 32;
+    float areg[NCH][8];
+    int areg_b = -1;
+    unsigned long long best = 0ull;
+    int cur = -1;
+    for (long long g = i0 + (long long)warp * kPoolRows; g < i1; g += (long long)nwarps * kPoolRows) {
+        const int nr = (int)min((long long)kPoolRows, i1 - g);
+        int v[kPoolRows];
+#pragma unroll
+        for (int rr = 0; rr < kPoolRows; ++rr) v[rr] = rr < nr ? pool[g + rr] : 0;
+        uint4 w[kPoolRows][NCH];
+#pragma unroll
+        for (int rr = 0; rr < kPoolRows; ++rr)
+#pragma unroll
+            for (int cc = 0; cc < NCH; ++cc) {
+                const int e = (lane + 32 * cc) * 8;
+                w[rr][cc] = (rr < nr && e < F) ? ldg_stream(fc2 + (size_t)v[rr] * F + e) : make_uint4(0, 0, 0, 0);
+            }
+        // the finishing lane of each row fetches its bias and base logit early
+        const int rsel = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+        const bool fin = (lane & 7) == 0 && rsel < nr;
+        float tail = 0.f;
+        int rb = 0, rv = 0;
+        if (fin) {
+            rb = (int)((g + rsel) / K);
+            rv = pool[g + rsel];
+            tail = __bfloat162float(bias[rv]) + L[((size_t)rb * kBlock + kRowOffset + k) * V + rv];
+        }
+        float part[kPoolRows];
+#pragma unroll
+        for (int rr = 0; rr < kPoolRows; ++rr) {
+            part[rr] = 0.f;
+            if (rr < nr) {
+                const int b = (int)((g + rr) / K);
+                if (b != areg_b) {  // warp-uniform, once per request run
+#pragma unroll
+                    for (int cc = 0; cc < NCH; ++cc) {
+                        const int e = (lane + 32 * cc) * 8;
+                        if (e < F) {
+                            const float4 x = __ldg(reinterpret_cast<const float4*>(a + (size_t)b * F + e));
+                            const float4 y = __ldg(reinterpret_cast<const float4*>(a + (size_t)b * F + e) + 1);
+                            areg[cc][0] = x.x; areg[cc][1] = x.y; areg[cc][2] = x.z; areg[cc][3] = x.w;
+                            areg[cc][4] = y.x; areg[cc][5] = y.y; areg[cc][6] = y.z; areg[cc][7] = y.w;
+                        }
+                    }
+                    areg_b = b;
+                }
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < NCH; ++cc) {
+                    const int e = (lane + 32 * cc) * 8;
+                    if (e < F) {
+                        float x[8];
+                        bf16x2_to_f32(w[rr][cc].x, x[0], x[1]);
+                        bf16x2_to_f32(w[rr][cc].y, x[2], x[3]);
+                        bf16x2_to_f32(w[rr][cc].z, x[4], x[5]);
+                        bf16x2_to_f32(w[rr][cc].w, x[6], x[7]);
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) {
+                            a0 = fmaf(x[i], areg[cc][i], a0);
+                            a1 = fmaf(x[i + 1], areg[cc][i + 1], a1);
+                        }
+                    }
+                }
+                part[rr] = a0 + a1;
+            }
+        }
+        const float tot = warp_sum4_t(part[0], part[1], part[2], part[3], lane);
+        if (fin) {
+            const float cv = tot + tail;
+            const unsigned long long key = pack_key(cv, (uint32_t)rv);
+            const int bl = rb - b_first;
+            if (bl != cur) {
+                if (cur >= 0 && best) atomicMax(&sbest[cur], best);
+                cur = bl;
+                best = 0ull;
+            }
+            best = key > best ? key : best;
+            if (dbg_scores) dbg_scores[((size_t)rb * kCorrected + (k - 1)) * K + (int)((g + rsel) % K)] = cv;
+        }
+    }
+    if (best) atomicMax(&sbest[cur], best);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nreq; i += blockDim.x)
+        if (sbest[i]) atomicMax(&keys[(size_t)(b_first + i) * kBlock + k], sbest[i]);
+}
+
 template <typename T>
 using GruKern = void (*)(const T*, const T*, const T*, const float*, float*, const int32_t*, const int32_t*,
                          const unsigned long long*, int*, int*, float*, int, int, int, int, int);
@@ -227,7 +362,34 @@ Fc1Kern<T> pick_fc1(int nch) {
 
 inline int nch_of(int n) { return (n + 255) / 256; }
 
+template <int NCH>
+cudaError_t launch_pool_nch(domino_ctx* c, RunArgs& r, int k) {
+    const domino_config& g = c->cfg;
+    // items per block: enough for 4 rows per warp and at most 64 requests a block
+    long long items = (long long)r.B * r.K;
+    int ipb = 8 * kPoolRows * 8;  // 8 groups per warp
+    if ((long long)ipb > 62LL * r.K) ipb = (int)(62LL * r.K);
+    if (ipb < 1) ipb = 1;
+    const long long blocks = (items + ipb - 1) / ipb;
+    k_correct_pool_batch<NCH><<<(unsigned)blocks, kBatchThreads, 0, r.st>>>(
+        (const __nv_bfloat16*)c->fc2, (const __nv_bfloat16*)c->bias, c->L, c->a, c->pool, c->keys, r.dbg.scores, k,
+        r.B, g.V, g.F, r.K, ipb);
+    ++r.launches;
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+bool pool_batch_supported(const domino_ctx* c) {
+    return c->cfg.dtype == DOMINO_DTYPE_BF16 && (c->cfg.F & 7) == 0 && nch_of(c->cfg.F) <= 8;
+}
+
+cudaError_t launch_correct_pool_batch(domino_ctx* c, RunArgs& r, int k) {
+    const int nch = nch_of(c->cfg.F);
+    return nch <= 1 ? launch_pool_nch<1>(c, r, k) : nch <= 2 ? launch_pool_nch<2>(c, r, k)
+         : nch <= 4 ? launch_pool_nch<4>(c, r, k) : nch <= 6 ? launch_pool_nch<6>(c, r, k)
+                    : launch_pool_nch<8>(c, r, k);
+}
 
 bool batch_kernels_supported(const domino_ctx* c) {
     const domino_config& g = c->cfg;

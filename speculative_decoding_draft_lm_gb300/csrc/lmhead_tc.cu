@@ -33,8 +33,10 @@ struct EpiLmHead {
         for (int b = t; b < n; b += 128)
             if (sb[b]) atomicMax(&keys[(size_t)b * kBlock], sb[b]);
     }
+    template <int PF>
+    __device__ __forceinline__ void prefetch(int, int, float*) const {}
     __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane,
-                                               unsigned long long* sb) const {
+                                               unsigned long long* sb, const float*) const {
         const int b = col0 >> 4;  // 16 columns = the 16 block rows of request b
         if (b >= B) return;       // uniform across the warp
         const bool ok = row < V;

@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
 
     // ------------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
-        if (lane == 0) {
+        if (lane < 4) {
             // full vocabulary: normal priority, so that the rows a step reads last
             // are still in L2 when the next step (walking backwards) starts;
             // pool rows are re-read every step: keep them
@@ -349,6 +349,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                     const int c = fwd ? ci : n_chunks - 1 - ci;
                     const int slot = q % p.n_slots;
                     const uint32_t par = (uint32_t)((q / p.n_slots) & 1);
+                    if ((q & 3) != lane) {  // four producer lanes share the issue work
+                        ++q;
+                        continue;
+                    }
                     if (!tc::mbar_wait(empty0 + 8 * slot, par ^ 1, abort_flag, p.err)) break;
                     const int r0 = c * kRowsPerSlot;
                     const int nr = min(kRowsPerSlot, nw - r0);
@@ -367,6 +371,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                     ++q;
                 }
             }
+            if (lane != 0) return;
             // every copy issued must land before the block exits
             const unsigned long long t0 = tc::globaltimer();
             while (*consumed_ptr < q && !*abort_flag && tc::globaltimer() - t0 < tc::kWaitLimitNs) {
@@ -715,6 +720,8 @@ struct Plan {
     int seg, slot_bytes, n_slots, n_cons, smem;
 };
 
+inline int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+
 // Per-CTA slice, ring slot size and ring depth: the ring gets what the rest
 // of the layout leaves of the opt-in shared-memory maximum (n_slots < 2: no).
 Plan make_plan(const domino_ctx* c, int B, int K) {
@@ -730,14 +737,18 @@ Plan make_plan(const domino_ctx* c, int B, int K) {
     Layout base(0, slot_bytes, g.E, g.G, g.F, seg, B, K);
     int n_slots = (max_smem - base.total - 1024) / (slot_bytes + 16);
     if (n_slots > kMaxSlots) n_slots = kMaxSlots;
+    // four producer lanes own the slots q % 4: keep the ring a multiple of 4;
     // consumer warps: the count (<= kConsumerWarps) whose multiple uses the most slots
     int n_cons = n_slots < kConsumerWarps ? n_slots : kConsumerWarps;
     int best = n_cons > 0 ? n_slots / n_cons * n_cons : 0;
-    for (int w = n_cons - 1; w >= 8; --w)
-        if (n_slots / w * w > best) {
-            best = n_slots / w * w;
+    best = 0;
+    for (int w = n_cons; w >= 4; --w) {
+        const int l = w * 4 / gcd_int(w, 4);  // lcm(w, 4)
+        if (n_slots / l * l > best) {
+            best = n_slots / l * l;
             n_cons = w;
         }
+    }
     Plan pl{seg, slot_bytes, best, n_cons, 0};
     n_slots = best;
     if (n_slots >= 2) pl.smem = Layout(n_slots, slot_bytes, g.E, g.G, g.F, seg, B, K).total;
