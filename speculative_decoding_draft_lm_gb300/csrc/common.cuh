@@ -51,6 +51,32 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k)
     }
     return k;
 }
+// Per-slot maxima of 16 keys over the warp with a transposed butterfly
+// (16 64-bit shuffles instead of 16 separate 5-level reductions).  Returns
+// the maximum of slot ((l>>4)&1)*8 + ((l>>3)&1)*4 + ((l>>2)&1)*2 + ((l>>1)&1)
+// in lane l (lanes l and l^1 hold the same slot).
+__device__ __forceinline__ unsigned long long warp_max16_u64(unsigned long long* v, int lane) {
+#pragma unroll
+    for (int level = 0; level < 4; ++level) {
+        const int mask = 16 >> level, half = 8 >> level;
+        const bool up = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < half) {
+                const unsigned long long send = up ? v[i] : v[i + half];
+                const unsigned long long keep = up ? v[i + half] : v[i];
+                const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, mask);
+                v[i] = got > keep ? got : keep;
+            }
+        }
+    }
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return other > v[0] ? other : v[0];
+}
+__device__ __forceinline__ int warp_max16_slot(int lane) {
+    return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -54,21 +54,23 @@ struct EpiCorrect {
                 base[j] = (ok && j < nb) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
         }
         const float bv = ok ? __bfloat162float(bias[row]) : 0.f;
+        unsigned long long kk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
+            kk[j] = 0ull;
+            if (ok && j < nb) {
+                const float c = v[j] + bv + base[j];
+                kk[j] = pack_key(c, (uint32_t)row);
+                if (dbg_scores) dbg_scores[((size_t)(col0 + j) * kCorrected + (k - 1)) * V + row] = c;
+            }
+        }
+        // the 32 rows' best per request, one request per lane pair
+        const unsigned long long key = warp_max16_u64(kk, lane);
+        const int j = warp_max16_slot(lane);
+        if ((lane & 1) == 0 && j < nb && key) {
             const int b = col0 + j;
-            if (j >= nb) break;  // uniform
-            float c = 0.f;
-            if (ok) {
-                c = v[j] + bv + base[j];
-                if (dbg_scores) dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + row] = c;
-            }
-            unsigned long long key = ok ? pack_key(c, (uint32_t)row) : 0ull;
-            key = warp_max_u64(key);
-            if (lane == 0 && key) {
-                if (b < tc::kEpiScratch) atomicMax(&sb[b], key);
-                else atomicMax(&keys[(size_t)b * kBlock + k], key);
-            }
+            if (b < tc::kEpiScratch) atomicMax(&sb[b], key);
+            else atomicMax(&keys[(size_t)b * kBlock + k], key);
         }
     }
 };
