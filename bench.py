@@ -41,8 +41,8 @@ SWEEP = ("qwen3_8b_b1_k0", "qwen3_8b_b8_k0", "qwen3_8b_b64_k0",
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_b1_k0", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-sweep", action="store_true", help="skip the B=1/8/64 x K0/K2048 table")
@@ -86,6 +86,13 @@ def alg_bytes(sh: inputs.Shape, B: int, K: int) -> dict:
 # ---- clocks sampler ---------------------------------------------------------
 
 class Clocks:
+    """SM clock and clock-event reasons sampled during the timed region.
+
+    Reads NVML through ctypes every ~2 ms from a background thread (read-only
+    queries); falls back to `nvidia-smi -lms 200` when NVML is unavailable.
+    """
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -94,8 +101,59 @@ class Clocks:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.nvml = None
+        self.handle = None
+        self.samples = []
+        self.stop_flag = False
+        self.thread = None
+        self._init_nvml()
+
+    def _init_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            import torch
+            props = torch.cuda.get_device_properties(self.dev)
+            handle = ctypes.c_void_p()
+            ok = False
+            bus = getattr(props, "pci_bus_id", None)
+            if bus is not None:
+                dom = getattr(props, "pci_domain_id", 0)
+                devid = getattr(props, "pci_device_id", 0)
+                busid = ("%08x:%02x:%02x.0" % (dom, bus, devid)).encode()
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(busid, ctypes.byref(handle)) == 0
+            if not ok:
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(self.dev, ctypes.byref(handle)) == 0
+            if ok:
+                self.nvml, self.handle = lib, handle
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def _poll(self):
+        import ctypes
+        lib, h = self.nvml, self.handle
+        clk = ctypes.c_uint()
+        mw = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                p_ok = lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0
+                r_ok = get_reasons(h, ctypes.byref(rs)) == 0
+                self.samples.append((clk.value, mw.value / 1000.0 if p_ok else None, rs.value if r_ok else 0))
+            time.sleep(0.002)
 
     def start(self):
+        if self.nvml is not None:
+            import threading
+            self.samples = []
+            self.stop_flag = False
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -106,6 +164,22 @@ class Clocks:
             self.proc = None
 
     def stop(self) -> dict:
+        if self.nvml is not None:
+            import ctypes
+            self.stop_flag = True
+            self.thread.join()
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))
+            sm = [x[0] for x in self.samples]
+            pw = [x[1] for x in self.samples if x[1] is not None]
+            reasons = set()
+            for _, _, r in self.samples:
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        reasons.add(name)
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx.value or None,
+                    "power_w_max": max(pw) if pw else None, "samples": len(sm), "source": "nvml, 2 ms",
+                    "reasons": sorted(reasons)}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -131,7 +205,8 @@ class Clocks:
                         reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+                "power_w_max": max(power) if power else None, "samples": len(sm), "source": "nvidia-smi, 200 ms",
+                "reasons": sorted(reasons)}
 
 
 # ---- distributed plumbing ---------------------------------------------------
@@ -145,46 +220,61 @@ def dist_env():
 
 # ---- CPU oracle leg ------------------------------------------------------------
 
-def oracle_sample(wl: inputs.Workload, weights: dict, requests: dict, budget_s: float) -> dict:
-    """Time the CPU oracle, as it stands, on a bounded slice of the workload.
+class OracleSample:
+    """The CPU oracle, as it stands, timed on a bounded slice of the workload.
 
     The oracle's cost is linear in the vocabulary (LM-head and correction), so
-    the sample keeps the first V_s vocabulary rows of lm_head/emb/fc2/b and the
-    first request, and the time is scaled by V / V_s to one block.  V_s is the
-    whole vocabulary when one block fits the budget.
+    a sample keeps the first V_s vocabulary rows of lm_head/emb/fc2/b and one
+    request, and its time is scaled by V / V_s to one block.  V_s is the whole
+    vocabulary when one block fits the per-step budget.  Widening the weights
+    to fp64 is the oracle's "load" and is done once, untimed.
     """
-    import numpy as np
-    import oracle
-    sh = wl.shape
-    req = {k: v[:1] for k, v in requests.items()}
 
-    def sliced(Vs):
+    def __init__(self, wl: inputs.Workload, weights: dict, requests: dict, budget_s: float):
+        import numpy as np
+        import oracle
+        self.oracle = oracle
+        self.wl = wl
+        sh = wl.shape
+        req = {k: v[:1] for k, v in requests.items()}
+        Vs = min(sh.V, 8192)
+        t = self._prepare_and_time(weights, req, Vs)
+        target = max(Vs, min(sh.V, int(Vs * budget_s / max(t, 1e-3))))
+        if target > Vs:
+            Vs = target
+            self._prepare_and_time(weights, req, Vs)
+        self.Vs = Vs
+        self.cores = len(os.sched_getaffinity(0))
+        self.sample = (f"1 request, vocabulary rows 0..{Vs - 1} of {sh.V} ({Vs / sh.V:.1%}), fp64 numpy/OpenBLAS, "
+                       f"time scaled by V/V_s to one block of {wl.B} request(s)")
+
+    def _prepare_and_time(self, weights, req, Vs):
+        import numpy as np
         w = dict(weights)
         for n in ("lm_head", "emb", "fc2", "b"):
             w[n] = weights[n][:Vs]
         r = dict(req)
         r["verified"] = (req["verified"] % Vs).astype(np.int32)
-        return w, r
+        self.Vs = Vs
+        self.ow = self.oracle.OracleWeights(w)
+        self.r = r
+        self.K = self.wl.K if self.wl.K < Vs else 0
+        return self.time_block() * Vs / self.wl.shape.V / self.wl.B
 
-    def timed(Vs):
-        w, r = sliced(Vs)
-        ow = oracle.OracleWeights(w)  # widening = loading, not timed
+    def time_block(self) -> float:
+        """Seconds for one block of the workload (all B requests), scaled."""
         t0 = time.perf_counter()
-        oracle.rollout(ow, r["hidden"], r["s"], r["verified"], wl.K if wl.K < Vs else 0)
-        return time.perf_counter() - t0
+        self.oracle.rollout(self.ow, self.r["hidden"], self.r["s"], self.r["verified"], self.K)
+        t = time.perf_counter() - t0
+        return t * self.wl.shape.V / self.Vs * self.wl.B
 
-    Vs = min(sh.V, 8192)
-    t = timed(Vs)
-    # grow the slice to use about half the budget
-    target = max(Vs, min(sh.V, int(Vs * (0.5 * budget_s) / max(t, 1e-3))))
-    if target > Vs:
-        Vs = target
-        t = timed(Vs)
-    per_block = t * sh.V / Vs
-    return {"value": 15.0 / per_block, "unit": UNIT, "s_per_block": per_block,
-            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"1 request, vocabulary rows 0..{Vs - 1} of {sh.V} "
-                      f"({Vs / sh.V:.1%}), fp64 numpy/OpenBLAS, time scaled by V/V_s to one block"}
+
+def oracle_sample(wl: inputs.Workload, weights: dict, requests: dict, budget_s: float) -> dict:
+    samp = OracleSample(wl, weights, requests, budget_s)
+    ts = [samp.time_block() for _ in range(2)]
+    s_block = min(ts)
+    return {"value": 15.0 * wl.B / s_block, "unit": UNIT, "s_per_block": s_block, "cores": samp.cores,
+            "kind": "oracle", "sample": samp.sample}
 
 
 def run_reference(args):
@@ -194,19 +284,19 @@ def run_reference(args):
         return 0
     wl = inputs.WORKLOADS[args.workload]
     weights, requests = inputs.make(wl, B=1)
-    budget = max(30.0, min(240.0, 8.0 * (args.steps + args.warmup)))
-    per_step_budget = budget / max(1, args.steps + args.warmup)
+    per_step = max(0.2, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    samp = OracleSample(wl, weights, requests, per_step)
     for _ in range(args.warmup):
-        oracle_sample(wl, weights, requests, per_step_budget)
-    vals = [oracle_sample(wl, weights, requests, per_step_budget) for _ in range(args.steps)]
-    s_per_block = statistics.median(v["s_per_block"] for v in vals) * wl.B
+        samp.time_block()
+    ts = [samp.time_block() for _ in range(args.steps)]
+    s_per_block = statistics.median(ts)
     value = 15.0 * wl.B / s_per_block
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_block * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(wl),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": vals[0]["cores"], "kind": "oracle",
-                             "sample": vals[0]["sample"] + f"; B={wl.B} requests scaled linearly"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": samp.cores, "kind": "oracle",
+                             "sample": samp.sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -270,13 +360,10 @@ def main():
     if eng.status() != 0:
         raise RuntimeError("device error during warm-up")
 
-    # timed region
-    eng.enable_timing(True)
-    eng.read_timing()
-    phase_ms = {}
-    phase_n = {}
-    launches = 0
+    # timed region: K steps, each bracketed by CUDA events on the launching
+    # stream, a 512 MiB write between steps so every step starts with a cold L2
     times = []
+    launches = 0
     clocks = Clocks(local)
     barrier()
     torch.cuda.synchronize()
@@ -291,15 +378,25 @@ def main():
         launches += eng.last_launch_count()
         e1.synchronize()
         times.append(e0.elapsed_time(e1))
-        for p, (ms, n) in eng.read_timing().items():
-            phase_ms[p] = phase_ms.get(p, 0.0) + ms
-            phase_n[p] = phase_n.get(p, 0) + n
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    eng.enable_timing(False)
     if eng.status() != 0:
         raise RuntimeError("device error during the timed steps")
+    # second timed region of K steps with the library's per-launch events (they
+    # separate consecutive launches, so they are kept out of the step time)
+    eng.enable_timing(True)
+    eng.read_timing()
+    phase_ms = {}
+    phase_n = {}
+    for _ in range(args.steps):
+        flush.zero_()
+        step(hid, s, ver, wl.B, wl.K)
+        torch.cuda.synchronize()
+        for p_, (ms, n) in eng.read_timing().items():
+            phase_ms[p_] = phase_ms.get(p_, 0.0) + ms
+            phase_n[p_] = phase_n.get(p_, 0) + n
+    eng.enable_timing(False)
     ms_step = sum(times) / len(times)
     if dist is not None:
         t = torch.tensor([ms_step], device="cuda")
@@ -361,6 +458,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s"}
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic, "kernel": dom,
                  "launches_per_step": phase_n[dom] / args.steps, "avg_launch_us": avg_ms * 1e3,
+                 "timing": "CUDA events around each launch on the run's stream, second timed region of K steps",
                  "alg_bytes_per_launch": ab.get(dom), "peak_source": peak_src + " (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback"})
     step_roof = {"alg_bytes_per_block": ab["block"],
@@ -392,12 +490,11 @@ def main():
             h2, s2, v2 = to_device(rq["hidden"]), to_device(rq["s"]), torch.from_numpy(rq["verified"]).cuda()
             for _ in range(3):
                 step(h2, s2, v2, w2.B, w2.K)
+            n_sweep = max(5, args.steps // 2)
+            # clean step times: no per-launch events (they would serialise the
+            # programmatically dependent launches of the batched driver)
             tt = []
-            eng.enable_timing(True)
-            eng.read_timing()
-            lm_ms, lm_n = 0.0, 0
-            ph_ms = {}
-            for _ in range(max(5, args.steps // 2)):
+            for _ in range(n_sweep):
                 flush.zero_()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -406,6 +503,15 @@ def main():
                 e1.record(stream)
                 e1.synchronize()
                 tt.append(e0.elapsed_time(e1))
+            # separate pass for the per-phase breakdown
+            eng.enable_timing(True)
+            eng.read_timing()
+            lm_ms, lm_n = 0.0, 0
+            ph_ms = {}
+            for _ in range(n_sweep):
+                flush.zero_()
+                step(h2, s2, v2, w2.B, w2.K)
+                torch.cuda.synchronize()
                 ph = eng.read_timing()
                 lm_ms += ph["lmhead"][0]
                 lm_n += ph["lmhead"][1]
@@ -420,7 +526,7 @@ def main():
                            "hbm_frac_block": ab2["block"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "lmhead_us": lm_avg * 1e3,
                            "lmhead_tensor_frac": ab2["lmhead_flop"] / (lm_avg * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                           "phase_us": {k_: m_ * 1e3 / len(tt) for k_, m_ in ph_ms.items()}}
+                           "phase_us_timed_pass": {k_: m_ * 1e3 / n_sweep for k_, m_ in ph_ms.items()}}
         torch.cuda.synchronize()
         if eng.status() != 0:
             raise RuntimeError("device error during the sweep")

@@ -85,6 +85,15 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel of the
+// stream is still running.  pdl_wait() blocks until that kernel has completed
+// and its memory is visible (a no-op for a normal launch); pdl_trigger() lets
+// the next kernel start early.  Everything before pdl_wait() may only touch
+// data no earlier kernel of the run writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // element loads: 8 consecutive elements widened to fp32
 __device__ __forceinline__ void load8(const float* p, float* o) {

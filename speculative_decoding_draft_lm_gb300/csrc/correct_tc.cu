@@ -89,9 +89,9 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) 
     const int tiles = ((c->cfg.V + tc::kBM - 1) / tc::kBM) * ((r.B + BN - 1) / BN);
     const int grid = tiles < c->num_sms ? tiles : c->num_sms;
     EpiCorrect epi{(const __nv_bfloat16*)c->bias, c->L, c->keys, r.dbg.scores, c->cfg.V, r.B, k};
-    kern<<<grid, tc::kGemmThreads, S::SMEM, r.st>>>(c->tm_fc2, tmB, c->cfg.V, r.B, c->cfg.F, epi, c->err);
     ++r.launches;
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_fc2, tmB, c->cfg.V, r.B,
+                      c->cfg.F, epi, c->err);
 }
 
 }  // namespace

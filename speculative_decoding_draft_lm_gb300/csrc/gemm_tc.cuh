@@ -91,6 +91,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // setup above overlaps the previous kernel; everything below may read its output
+    pdl_trigger();
+    pdl_wait();
 
     const int m_tiles = (M + kBM - 1) / kBM;
     const int n_tiles = (N + BN - 1) / BN;

@@ -118,10 +118,13 @@ __global__ void __launch_bounds__(kBatchThreads) k_gru_batch(
     const int jn = min(kJT, G - j0);
     T* s_ih = reinterpret_cast<T*>(smem);                      // [3*jn][E]
     T* s_hh = s_ih + (size_t)3 * kJT * E;                      // [3*jn][G]
+    pdl_trigger();
+    // weights do not depend on the previous kernel: stage them before waiting
     stage_rows(s_ih, w_ih, j0, jn, G, E);
     if (u > 0) stage_rows(s_hh, w_hh, j0, jn, G, G);
     cp_wait();
     __syncthreads();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int b = warp; b < B; b += kBatchThreads / 32) {
         int t;
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(kBatchThreads) k_fc1_batch(const T* __restrict
     const int f0 = blockIdx.x * kFT;
     const int fn = min(kFT, F - f0);
     T* s_w = reinterpret_cast<T*>(smem);  // [fn][G]
+    pdl_trigger();
     const int per_row = G * (int)sizeof(T) / 16;
     for (int i = threadIdx.x; i < fn * per_row; i += blockDim.x) {
         const int rr = i / per_row, e = (i % per_row) * (16 / (int)sizeof(T));
@@ -186,6 +190,7 @@ __global__ void __launch_bounds__(kBatchThreads) k_fc1_batch(const T* __restrict
     }
     cp_wait();
     __syncthreads();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int b = warp; b < B; b += kBatchThreads / 32) {
         VecRegs<T, NCH> hv;
@@ -247,6 +252,8 @@ __global__ void __launch_bounds__(kBatchThreads) k_correct_pool_batch(
     const float* __restrict__ a, const int32_t* __restrict__ pool, unsigned long long* __restrict__ keys,
     float* __restrict__ dbg_scores, int k, int B, int V, int F, int K, int items_per_block) {
     __shared__ unsigned long long sbest[64];
+    pdl_trigger();
+    pdl_wait();
     const long long items = (long long)B * K;
     const long long i0 = (long long)blockIdx.x * items_per_block;
     const long long i1 = min(items, i0 + items_per_block);
@@ -371,11 +378,11 @@ cudaError_t launch_pool_nch(domino_ctx* c, RunArgs& r, int k) {
     if ((long long)ipb > 62LL * r.K) ipb = (int)(62LL * r.K);
     if (ipb < 1) ipb = 1;
     const long long blocks = (items + ipb - 1) / ipb;
-    k_correct_pool_batch<NCH><<<(unsigned)blocks, kBatchThreads, 0, r.st>>>(
-        (const __nv_bfloat16*)c->fc2, (const __nv_bfloat16*)c->bias, c->L, c->a, c->pool, c->keys, r.dbg.scores, k,
-        r.B, g.V, g.F, r.K, ipb);
     ++r.launches;
-    return cudaGetLastError();
+    return launch_pdl(k_correct_pool_batch<NCH>, dim3((unsigned)blocks), dim3(kBatchThreads), 0, r.st,
+                      (const __nv_bfloat16*)c->fc2, (const __nv_bfloat16*)c->bias, (const float*)c->L,
+                      (const float*)c->a, (const int32_t*)c->pool, c->keys, r.dbg.scores, k, r.B, g.V, g.F, r.K,
+                      ipb);
 }
 
 }  // namespace
@@ -412,11 +419,10 @@ cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (g.G + kJT - 1) / kJT;
-    kern<<<grid, kBatchThreads, smem, r.st>>>((const T*)c->emb, (const T*)c->w_ih, (const T*)c->w_hh, h_in, h_out,
-                                              r.verified, r.forced, c->keys, c->bad, c->err, r.dbg.h, u, r.B, g.V,
-                                              g.E, g.G);
     ++r.launches;
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kBatchThreads), smem, r.st, (const T*)c->emb, (const T*)c->w_ih,
+                      (const T*)c->w_hh, h_in, h_out, r.verified, r.forced, (const unsigned long long*)c->keys, c->bad,
+                      c->err, r.dbg.h, u, r.B, g.V, g.E, g.G);
 }
 
 cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k) {
@@ -428,10 +434,9 @@ cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (g.F + kFT - 1) / kFT;
-    kern<<<grid, kBatchThreads, smem, r.st>>>((const T*)c->fc1, h, (const T*)r.s, c->a, c->a16, r.dbg.z, k, r.B,
-                                              g.G, g.F);
     ++r.launches;
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kBatchThreads), smem, r.st, (const T*)c->fc1, h, (const T*)r.s, c->a,
+                      c->a16, r.dbg.z, k, r.B, g.G, g.F);
 }
 
 }  // namespace domino

@@ -21,6 +21,8 @@ inline int grid_for(int items_per_block_unit, int units, int cap) {
 // ---------------------------------------------------------------------------
 __global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__ bad, unsigned* __restrict__ sync,
                         int n_keys, int B) {
+    pdl_trigger();
+    pdl_wait();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n_keys) keys[i] = 0ull;
     if (i < B) bad[i] = 0;
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(256) k_correct_pool(const T* __restrict__ fc2,
 // ---------------------------------------------------------------------------
 __global__ void k_finalize(const unsigned long long* __restrict__ keys, const int* __restrict__ bad,
                            int32_t* __restrict__ out, float* __restrict__ dbg_top1, int B) {
+    pdl_wait();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= B * kProposals) return;
     int b = i / kProposals, j = i % kProposals;
@@ -400,9 +403,8 @@ __global__ void k_finalize(const unsigned long long* __restrict__ keys, const in
 
 cudaError_t launch_reset(domino_ctx* c, RunArgs& r) {
     int n = r.B * kBlock;
-    k_reset<<<(n + 255) / 256, 256, 0, r.st>>>(c->keys, c->bad, c->sync, n, r.B);
-    DOMINO_LAUNCH_CHECK();
-    return cudaSuccess;
+    ++r.launches;
+    return launch_pdl(k_reset, dim3((n + 255) / 256), dim3(256), 0, r.st, c->keys, c->bad, c->sync, n, r.B);
 }
 
 cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r) {
@@ -493,9 +495,9 @@ cudaError_t launch_correct_simt(domino_ctx* c, RunArgs& r, int k) {
 
 cudaError_t launch_finalize(domino_ctx* c, RunArgs& r) {
     int n = r.B * kProposals;
-    k_finalize<<<(n + 255) / 256, 256, 0, r.st>>>(c->keys, c->bad, r.out_tokens, r.dbg.top1, r.B);
-    DOMINO_LAUNCH_CHECK();
-    return cudaSuccess;
+    ++r.launches;
+    return launch_pdl(k_finalize, dim3((n + 255) / 256), dim3(256), 0, r.st, (const unsigned long long*)c->keys,
+                      (const int*)c->bad, r.out_tokens, r.dbg.top1, r.B);
 }
 
 // The full-vocabulary correction kernel needs NB*F*4 bytes of dynamic shared

@@ -88,9 +88,9 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, float* 
     const int tiles = ((c->cfg.V + tc::kBM - 1) / tc::kBM) * ((N + BN - 1) / BN);
     const int grid = tiles < c->num_sms ? tiles : c->num_sms;
     EpiLmHead epi{c->L, c->keys, score, c->cfg.V, r.B};
-    kern<<<grid, tc::kGemmThreads, S::SMEM, r.st>>>(c->tm_lm_head, tmB, c->cfg.V, N, c->cfg.H, epi, c->err);
     ++r.launches;
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_lm_head, tmB, c->cfg.V, N,
+                      c->cfg.H, epi, c->err);
 }
 
 }  // namespace
