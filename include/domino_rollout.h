@@ -52,6 +52,7 @@ extern "C" {
 #define DOMINO_ERR_OOM           -5  /* workspace allocation failed                  */
 #define DOMINO_ERR_TIMEOUT       -6  /* a device-side wait hit its iteration limit   */
 #define DOMINO_ERR_BAD_TOKEN     -7  /* verified/forced token outside [0, V)         */
+#define DOMINO_ERR_SCRATCH_LIMIT -8  /* request larger than the static scratch        */
 
 #define DOMINO_DTYPE_FP32 0  /* fp32 weights/activations, fp32 arithmetic          */
 #define DOMINO_DTYPE_BF16 1  /* bf16 weights/activations, fp32 accumulation        */
@@ -161,6 +162,32 @@ DOMINO_API int domino_rollout_status(domino_ctx* ctx, void* cuda_stream);
 
 /* Number of kernel launches the last run()/debug_run() enqueued. */
 DOMINO_API int domino_rollout_last_launch_count(const domino_ctx* ctx);
+
+/* Allocation-free candidate pool.  The method described by the pages has no
+ * counterpart for this entry point: it exists for callers that must not
+ * allocate device memory, e.g. code that runs while a memory planner owns
+ * every byte of the device, or a process whose allocator is locked for the
+ * lifetime of a captured workload.  It needs no context and calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *
+ * From base logits [B,16,V] fp32 (DEVICE, caller-owned; the layout that
+ * domino_rollout_debug_run dumps), it forms score[b,v] = max over rows 1..15
+ * in a scratch array that the library keeps in a file-scope __device__
+ * buffer of DOMINO_STATIC_SCRATCH_FLOATS floats (8 MiB on every device that
+ * loads the library, held until the process exits), then writes the K ids
+ * with the largest scores (ties to the lower id), ascending, to pool_out
+ * [B,K] int32 (DEVICE, caller-owned) on `cuda_stream`, for the current device.
+ *
+ * The first call on a device looks up the buffer's device address on that
+ * device; make that first call before any stream capture.  All calls share
+ * the one buffer and every call overwrites it, so calls whose kernels can
+ * overlap on the GPU (different streams without ordering) race and must be
+ * serialised by the caller.  Requires 0 < K < V and V <= 431000.  Errors:
+ * INVALID_ARG (null pointer, B < 1, K outside (0, V), V too large),
+ * SCRATCH_LIMIT (B * V > DOMINO_STATIC_SCRATCH_FLOATS), CUDA. */
+#define DOMINO_STATIC_SCRATCH_FLOATS (2u * 1024u * 1024u)
+DOMINO_API int domino_candidate_pool_static(const float* base_logits, int B, int V, int K, int32_t* pool_out,
+                                            void* cuda_stream);
 
 /* Free the workspace and the context (NULL is ignored).  Synchronises the
  * context's device first.  Weights stay the caller's. */

@@ -333,6 +333,7 @@ const char* domino_rollout_strerror(int st) {
         case DOMINO_ERR_OOM: return "out of device memory";
         case DOMINO_ERR_TIMEOUT: return "device-side wait timed out";
         case DOMINO_ERR_BAD_TOKEN: return "token id outside [0, V)";
+        case DOMINO_ERR_SCRATCH_LIMIT: return "request exceeds the static scratch buffer";
         default: return "unknown status";
     }
 }

@@ -64,6 +64,8 @@ cudaError_t launch_correct_tc(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB,
 // cluster radix-select candidate pool (pool.cu)
 bool pool_cluster_supported(const domino_ctx* c);
 cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r);
+cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, int V, int K, cudaStream_t st);
+bool pool_cluster_fits(int V);
 
 // batched GRU / projector layer 1 for B >= 2 (kernels_batch.cu)
 bool batch_kernels_supported(const domino_ctx* c);

@@ -213,6 +213,32 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
 
 }  // namespace
 
+// Pool selection from caller-given scores: the same kernel, pointers passed in.
+cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, int V, int K, cudaStream_t st) {
+    const int chunk = (V + kRanks - 1) / kRanks;
+    const size_t smem = sizeof(PoolShared) + (size_t)chunk * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_pool_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kRanks, B);
+    cfg.blockDim = dim3(kPoolThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kRanks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_pool_cluster, score, pool, V, K, chunk);
+}
+
+bool pool_cluster_fits(int V) {
+    const int chunk = (V + kRanks - 1) / kRanks;
+    return sizeof(PoolShared) + (size_t)chunk * 4 <= 220 * 1024;
+}
+
 bool pool_cluster_supported(const domino_ctx* c) {
     const int chunk = (c->cfg.V + kRanks - 1) / kRanks;
     return sizeof(PoolShared) + (size_t)chunk * 4 <= 220 * 1024;

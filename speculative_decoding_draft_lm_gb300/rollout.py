@@ -21,6 +21,8 @@ DOMINO_ERR_CUDA = -4
 DOMINO_ERR_OOM = -5
 DOMINO_ERR_TIMEOUT = -6
 DOMINO_ERR_BAD_TOKEN = -7
+DOMINO_ERR_SCRATCH_LIMIT = -8
+DOMINO_STATIC_SCRATCH_FLOATS = 2 * 1024 * 1024
 
 DOMINO_DTYPE_FP32 = 0
 DOMINO_DTYPE_BF16 = 1
@@ -35,7 +37,7 @@ EXPORTED = (
     "domino_rollout_init", "domino_rollout_load_weights", "domino_rollout_run",
     "domino_rollout_debug_run", "domino_rollout_set_driver", "domino_rollout_status",
     "domino_rollout_last_launch_count", "domino_rollout_destroy", "domino_rollout_strerror",
-    "domino_rollout_enable_timing", "domino_rollout_read_timing",
+    "domino_rollout_enable_timing", "domino_rollout_read_timing", "domino_candidate_pool_static",
 )
 
 PHASES = ("lmhead", "argmax", "pool", "gru", "fc1", "correct", "steps", "other")
@@ -86,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.domino_rollout_destroy.restype = None
     lib.domino_rollout_enable_timing.argtypes = [vp, i]
     lib.domino_rollout_read_timing.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
+    lib.domino_candidate_pool_static.argtypes = [vp, i, i, i, vp, vp]
     lib.domino_rollout_strerror.argtypes = [i]
     lib.domino_rollout_strerror.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -168,6 +171,11 @@ def domino_rollout_read_timing(ctx) -> dict:
     n = (ctypes.c_int * len(PHASES))()
     _check(load_library().domino_rollout_read_timing(ctx, ms, n), "domino_rollout_read_timing")
     return {p: (float(ms[i]), int(n[i])) for i, p in enumerate(PHASES)}
+
+
+def domino_candidate_pool_static(base_logits, B: int, V: int, K: int, pool_out, stream=None) -> int:
+    """Allocation-free pool selection (see the header): returns the status."""
+    return load_library().domino_candidate_pool_static(_ptr(base_logits), B, V, K, _ptr(pool_out), _stream(stream))
 
 
 def domino_rollout_destroy(ctx) -> None:
