@@ -26,7 +26,7 @@ __global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n_keys) keys[i] = 0ull;
     if (i < B) bad[i] = 0;
-    if (i < 4) sync[i] = 0u;
+    if (i < 64) sync[i] = 0u;  // grid-barrier counter and the per-step chunk counters
 }
 
 // ---------------------------------------------------------------------------

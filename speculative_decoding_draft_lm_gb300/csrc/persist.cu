@@ -335,8 +335,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     }
     __syncthreads();
 
+    // This kernel may start while the previous kernel of the stream (the
+    // LM-head, or the pool selection) still runs: pdl_wait() separates what
+    // only reads weights and inputs from what reads that kernel's output.
+    pdl_trigger();
     // ------------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
+        if (!full_vocab) pdl_wait();  // pool ids come from the previous kernel
         if (lane < 4) {
             // full vocabulary: normal priority, so that the rows a step reads last
             // are still in L2 when the next step (walking backwards) starts;
@@ -390,6 +395,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     }
 
     // ------------------------------------------------------------------ consumers
+    if (!full_vocab) pdl_wait();
     unsigned nsync = 0;
     unsigned* counter = p.sync;
     // static per-CTA bias values of the slice
@@ -687,8 +693,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     };
     auto body = [&]() {
         stamp();                                                     // 0: start
-        gru(0, false);
+        gru(0, false);  // the verified token: independent of the previous kernel
         stamp();                                                     // 1
+        pdl_wait();     // base logits, p_1 and the cleared argmax words are ready
         if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
         stamp();                                                     // 2
         gru(1, false);
@@ -829,11 +836,13 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     cfg.blockDim = dim3(kPersistThreads);
     cfg.dynamicSmemBytes = lay.total;
     cfg.stream = r.st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, p);
     ++r.launches;
     return e;
