@@ -271,7 +271,7 @@ __host__ __device__ inline int phase_c_requests(int B, int K, int seg) {
 }
 
 struct Layout {
-    int ring, bars, sa, sx, sh, sg, sL, sbias, sbest, stok, misc, total;
+    int ring, bars, sa, sx, sh, sg, sL, sbias, stot, sbest, stok, misc, total;
     __host__ __device__ Layout(int n_slots, int slot_bytes, int E, int G, int F, int seg, int B, int K) {
         auto up = [](int x) { return (x + 127) & ~127; };
         const int nreq = phase_c_requests(B, K, seg), ngru = B < kGruGroup ? B : kGruGroup;
@@ -284,6 +284,7 @@ struct Layout {
         sg = o;   o = up(o + 4 * 9 * kGruGroup * 64);   // gate products + next hidden-side products
         sL = o;   o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
+        stot = o; o = up(o + 4 * seg);
         sbest = o; o = up(o + 8 * kMaxReq);
         stok = o; o = up(o + 4 * 256);
         misc = o; o = up(o + 64);
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     float* sg = reinterpret_cast<float*>(sm + lay.sg);
     float* sL = reinterpret_cast<float*>(sm + lay.sL);
     float* sbias = reinterpret_cast<float*>(sm + lay.sbias);
+    float* stot = reinterpret_cast<float*>(sm + lay.stot);  // fc2 row . a of each row of the slice
     unsigned long long* sbest = reinterpret_cast<unsigned long long*>(sm + lay.sbest);
     int* stok = reinterpret_cast<int*>(sm + lay.stok);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + lay.misc);
@@ -629,28 +631,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);  // the slot is read: hand it back
             const float tot = warp_sum4(part[0], part[1], part[2], part[3], lane);
             const int rsel = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            if ((lane & 7) == 0 && rsel < nr) {  // four lanes finish four rows
-                const int r = r0 + rsel;
-                const long long item = w0 + r;
-                const int bl = full_vocab ? 0 : (int)(item / p.K) - b_first;
-                const int v = full_vocab ? (int)item : p.pool[item];
-                const float cv = tot + sbias[r] + sL[r];
-                const unsigned long long key = pack_key(cv, (uint32_t)v);
-                if (bl != cur) {
-                    if (cur >= 0 && best) atomicMax(&sbest[cur], best);
-                    cur = bl;
-                    best = 0ull;
-                }
-                best = key > best ? key : best;
-                if (p.dbg_scores) {
-                    const int b = b_first + bl;
-                    if (full_vocab) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
-                    else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
-                }
-            }
+            if ((lane & 7) == 0 && rsel < nr) stot[r0 + rsel] = tot;  // finished after the loop
             if (lane == 0) atomicAdd((int*)consumed_ptr, 1);
         }
-        if (best) atomicMax(&sbest[cur], best);
         // hidden-side GRU products for the next update while the ring refills
         if (pre_gh && k < kCorrected && !*abort_flag) {
             for (int it = warp; it < jn * 3; it += kConsumerWarps) {
@@ -665,6 +648,32 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                     }
                 }
             }
+        }
+        cons_sync();
+        // finish every row of the slice: bias, base logit, argmax key
+        for (int r = tid; r < nw; r += kConsumerWarps * 32) {
+            const long long item = w0 + r;
+            const int bl = full_vocab ? 0 : (int)(item / p.K) - b_first;
+            const int v = full_vocab ? (int)item : p.pool[item];
+            const float cv = stot[r] + sbias[r] + sL[r];
+            const unsigned long long key = pack_key(cv, (uint32_t)v);
+            if (bl != cur) {
+                if (cur >= 0 && best) atomicMax(&sbest[cur], best);
+                cur = bl;
+                best = 0ull;
+            }
+            best = key > best ? key : best;
+            if (p.dbg_scores) {
+                const int b = b_first + bl;
+                if (full_vocab) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * V + v] = cv;
+                else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
+            }
+        }
+        if (full_vocab) {  // one request: reduce over the warp first
+            best = warp_max_u64(best);
+            if (lane == 0 && best) atomicMax(&sbest[0], best);
+        } else if (best) {
+            atomicMax(&sbest[cur], best);
         }
         cons_sync();
         if (tid < b_count) {
