@@ -218,6 +218,26 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_seeds(wl: inputs.Workload, rank: int) -> list:
+    """Request seeds of one replica: every rank runs its own B requests."""
+    return [s + rank * 100000 for s in wl.request_seeds]
+
+
+def max_over_ranks(x: float, dist, device: str) -> float:
+    """The slowest rank's value (identity without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(B: int, world: int, ms_per_step: float) -> float:
+    """Proposals per second of all replicas: 15 per request per block."""
+    return 15.0 * B * world / (ms_per_step * 1e-3)
+
+
 # ---- CPU oracle leg ------------------------------------------------------------
 
 class OracleSample:
@@ -338,8 +358,7 @@ def main():
     max_K = max([wl.K] + [inputs.WORKLOADS[n].K for n in sweep])
     weights = inputs.make_weights(sh, wl.weight_seed, wl.scales)
     # every rank runs its own requests (weak scaling of independent replicas)
-    seeds = [s + rank * 100000 for s in wl.request_seeds]
-    requests = inputs.make_requests(sh, seeds)
+    requests = inputs.make_requests(sh, replica_seeds(wl, rank))
 
     eng = DominoRollout(sh.V, sh.H, sh.E, sh.G, sh.F, max_B=max_B, max_K=max_K, dtype=sh.dtype, device=local)
     dw = {k: to_device(v) for k, v in weights.items()}
@@ -397,12 +416,8 @@ def main():
             phase_ms[p_] = phase_ms.get(p_, 0.0) + ms
             phase_n[p_] = phase_n.get(p_, 0) + n
     eng.enable_timing(False)
-    ms_step = sum(times) / len(times)
-    if dist is not None:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = 15.0 * wl.B * ws / (ms_step * 1e-3)
+    ms_step = max_over_ranks(sum(times) / len(times), dist, "cuda")
+    value = whole_job_rate(wl.B, ws, ms_step)
 
     # end to end through the public API: pinned host inputs -> run -> tokens back
     h_host = torch.from_numpy(requests["hidden"].view(np.int16) if requests["hidden"].dtype == np.uint16
@@ -431,11 +446,7 @@ def main():
         e1.synchronize()
         if i >= args.warmup:
             e2e_times.append(e0.elapsed_time(e1))
-    e2e_ms = sum(e2e_times) / len(e2e_times)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), dist, "cuda")
     h2d = h_host.numel() * h_host.element_size() + s_host.numel() * s_host.element_size() + v_host.numel() * 4
     d2h = o_host.numel() * 4
 
@@ -472,7 +483,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": sh.dtype,
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden/s, uniform verified token)",
             "config": workload_config(wl),
-            "e2e": {"value": 15.0 * wl.B * ws / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+            "e2e": {"value": whole_job_rate(wl.B, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches, "clocks": clk, "roofline": roof, "step_roofline": step_roof,
             "phase_share": shares,
