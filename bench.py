@@ -63,8 +63,9 @@ def load_peaks():
 
 # ---- algorithmic bytes / flops -------------------------------------------
 
-def alg_bytes(sh: inputs.Shape, B: int, K: int) -> dict:
-    """Algorithmic bytes per launch of each phase and per block (see DESIGN)."""
+def alg_bytes(sh: inputs.Shape, B: int, K: int, n_prop: int = 15) -> dict:
+    """Algorithmic bytes per launch of each phase and per block; ``n_prop``
+    proposals take max(2, n_prop) GRU updates and n_prop - 1 corrected steps."""
     e = 2 if sh.dtype == "bf16" else 4
     V, H, E, G, F = sh.V, sh.H, sh.E, sh.G, sh.F
     full = K == 0 or K >= V
@@ -76,8 +77,8 @@ def alg_bytes(sh: inputs.Shape, B: int, K: int) -> dict:
     gru = 3 * G * (E + G) * e + B * (E * e + G * 4 * 2)
     fc1 = F * G * e + B * (G * 4 + F * e + F * 4 * 2)
     pool = 0 if full else B * 15 * V * 4 + B * V * 4 * 5 + B * K * 4
-    # persistent driver: the GRU seed and 14 corrected steps in one launch
-    steps = 15 * gru + 14 * (fc1 + corr)
+    # persistent driver: the GRU seed and the corrected steps in one launch
+    steps = max(2, n_prop) * gru + (n_prop - 1) * (fc1 + corr)
     per_block = lm + pool + steps
     return {"lmhead": lm, "correct": corr, "gru": gru, "fc1": fc1, "pool": pool, "steps": steps,
             "block": per_block, "lmhead_flop": 2.0 * B * 16 * V * H}
@@ -492,11 +493,13 @@ def main():
                                               "B1_K2048": 1.618, "B8_K2048": 2.122, "B64_K2048": 7.188},
                         "note": "A100 numbers at the pages' checkpoint shapes; context only"}}
 
-    # B = 1/8/64 x K0/K2048 table on the same weights (rank 0)
+    # B = 1/8/64 x K0/K2048 table on the same weights (rank 0), then the
+    # early-stopped b8 variant (7 proposals) of the B = 1/8 workloads
     if sweep:
         table = {}
-        for name in sweep:
+        for name, n_prop in [(n, 15) for n in sweep] + [(n, 7) for n in sweep if inputs.WORKLOADS[n].B <= 8]:
             w2 = inputs.WORKLOADS[name]
+            eng.set_proposals(n_prop)
             rq = inputs.make_requests(sh, list(w2.request_seeds))
             h2, s2, v2 = to_device(rq["hidden"]), to_device(rq["s"]), torch.from_numpy(rq["verified"]).cuda()
             for _ in range(3):
@@ -531,13 +534,16 @@ def main():
                         ph_ms[k_] = ph_ms.get(k_, 0.0) + m_
             eng.enable_timing(False)
             ms = sum(tt) / len(tt)
-            ab2 = alg_bytes(sh, w2.B, w2.K)
+            ab2 = alg_bytes(sh, w2.B, w2.K, n_prop)
             lm_avg = lm_ms / max(1, lm_n)
-            table[name] = {"us_per_block": ms * 1e3, "proposals_per_s": 15.0 * w2.B / (ms * 1e-3),
-                           "hbm_frac_block": ab2["block"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                           "lmhead_us": lm_avg * 1e3,
-                           "lmhead_tensor_frac": ab2["lmhead_flop"] / (lm_avg * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                           "phase_us_timed_pass": {k_: m_ * 1e3 / n_sweep for k_, m_ in ph_ms.items()}}
+            table[name if n_prop == 15 else f"{name}_n{n_prop}"] = {
+                "us_per_block": ms * 1e3, "proposals": n_prop,
+                "proposals_per_s": float(n_prop) * w2.B / (ms * 1e-3),
+                "hbm_frac_block": ab2["block"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "lmhead_us": lm_avg * 1e3,
+                "lmhead_tensor_frac": ab2["lmhead_flop"] / (lm_avg * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                "phase_us_timed_pass": {k_: m_ * 1e3 / n_sweep for k_, m_ in ph_ms.items()}}
+        eng.set_proposals(15)
         torch.cuda.synchronize()
         if eng.status() != 0:
             raise RuntimeError("device error during the sweep")

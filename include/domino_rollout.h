@@ -155,6 +155,18 @@ DOMINO_API int domino_rollout_set_driver(domino_ctx* ctx, int driver);
 DOMINO_API int domino_rollout_enable_timing(domino_ctx* ctx, int enable);
 DOMINO_API int domino_rollout_read_timing(domino_ctx* ctx, float* ms, int* launches);
 
+/* Early stop: produce only the first n proposals (1 <= n <= 15; default 15)
+ * with n-1 corrected steps, for a target that verifies only the first n+1
+ * block positions (page "feat: support tensor-parallel Domino rollout",
+ * section "Qwen3.6-27B checkpoint and full serving benchmark": the b8 run
+ * keeps the block-16 draft and verifies 8 positions, i.e. n = 7).  The draft
+ * itself is unchanged: the LM-head still covers all 16 rows and the pool
+ * (K > 0) is still taken over the whole block, so the n tokens equal the
+ * first n of the full rollout.  out_tokens keeps its [B,15] layout; entries
+ * n..14 of each row are set to -1.  The setting applies to later runs of
+ * this context.  Errors: INVALID_ARG (null ctx or n outside 1..15). */
+DOMINO_API int domino_rollout_set_proposals(domino_ctx* ctx, int n);
+
 /* Synchronise `cuda_stream`, then return and clear the device error word
  * (DOMINO_OK, DOMINO_ERR_BAD_TOKEN or DOMINO_ERR_TIMEOUT), or DOMINO_ERR_CUDA
  * if the stream reported an error. */

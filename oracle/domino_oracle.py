@@ -141,7 +141,7 @@ class OracleWeights:
 
 
 def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
-            keep_scores: bool = False) -> dict:
+            keep_scores: bool = False, n_proposals: int = N_PROPOSALS) -> dict:
     """Run the Domino rollout for a batch of independent requests.
 
     ``hidden`` [B,16,H], ``s`` [B,15,F], ``verified`` [B] int.  ``forced``
@@ -149,12 +149,24 @@ def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
     ``forced[:, k]`` instead of the rollout's own choice, while the rollout's
     own argmax is still reported in ``tokens``.
 
+    ``n_proposals`` (1..15) stops the chain after that many proposals, as
+    for a target that verifies only the first n+1 block positions (page
+    "feat: support tensor-parallel Domino rollout", section "Qwen3.6-27B
+    checkpoint and full serving benchmark": b8 verifies 8 positions, n = 7,
+    with the block-16 draft unchanged).  The draft is not shortened: the
+    LM-head covers all 16 rows and the pool is still taken over rows 1..15.
+    ``tokens`` entries from n on are -1; ``h``, ``z``, ``margin``, ``top1``
+    keep their shapes with the unused entries left at zero.
+
     Returns a dict with ``tokens`` [B,15], ``L`` [B,16,V], ``pool`` (list of
     id arrays), ``h`` [B,15,G] (state after each of the 15 GRU updates),
     ``z`` [B,14,F] (pre-activation of each corrected step), ``margin`` [B,15]
     (top-1 minus top-2 score of every proposal), ``top1`` [B,15] (winning
     score) and, with ``keep_scores``, ``c`` (per request, [14, |pool|]).
     """
+    if not 1 <= n_proposals <= N_PROPOSALS:
+        raise ValueError("n_proposals must lie in 1..%d" % N_PROPOSALS)
+    n_corr = n_proposals - 1
     B = hidden.shape[0]
     L = lm_head(hidden, W.lm_head)                     # [B,16,V]
     s64 = widen(s)
@@ -186,7 +198,7 @@ def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
     hs[:, 1] = h
 
     full = all(len(p) == W.V for p in pools)
-    for k in range(1, N_CORRECTED + 1):
+    for k in range(1, n_corr + 1):
         z = h @ W.fc1.T + s64[:, k]
         zs[:, k - 1] = z
         a = silu(z)
@@ -205,14 +217,15 @@ def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
             top1[r, k] = c[j]
             if keep_scores:
                 scores[r].append(c.copy())
-        if k < N_CORRECTED:
+        if k < n_corr:
             h = gru_cell(W.emb[[fed(r, k) for r in range(B)]], h, W.w_ih, W.w_hh)
             hs[:, k + 1] = h
 
+    tokens[:, n_proposals:] = -1
     out = {"tokens": tokens, "L": L, "pool": pools, "h": hs, "z": zs,
            "margin": margin, "top1": top1}
     if keep_scores:
-        out["c"] = [np.stack(sc) for sc in scores]
+        out["c"] = [np.stack(sc) if sc else np.zeros((0, len(p))) for sc, p in zip(scores, pools)]
     return out
 
 

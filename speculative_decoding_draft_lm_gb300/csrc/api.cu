@@ -78,6 +78,7 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     r.verified = verified;
     r.B = B;
     r.K = Keff;
+    r.n_prop = c->n_proposals;
     r.forced = forced;
     if (dbg) r.dbg = *dbg;
     r.out_tokens = out;
@@ -129,7 +130,8 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
             e = prepare_correct_tc(c, r, &tm_a);
             if (e != cudaSuccess) goto fail;
         }
-        for (int k = 1; k <= kCorrected; ++k) {
+        const int n_corr = r.n_prop - 1;
+        for (int k = 1; k <= n_corr; ++k) {
             STEP(DOMINO_PHASE_FC1, FC1(k));
             if (tc_corr)
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_tc(c, r, tm_a, k));
@@ -137,7 +139,7 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_pool_batch(c, r, k));
             else
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
-            if (k < kCorrected) STEP(DOMINO_PHASE_GRU, GRU(k + 1));
+            if (k < n_corr) STEP(DOMINO_PHASE_GRU, GRU(k + 1));
         }
     }
 #undef GRU
@@ -222,6 +224,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
         return DOMINO_ERR_CUDA;
     }
     c->driver = DOMINO_DRIVER_AUTO;
+    c->n_proposals = kProposals;
     *out = c;
     return DOMINO_OK;
 }
@@ -295,6 +298,12 @@ int domino_rollout_read_timing(domino_ctx* c, float* ms, int* launches) {
         }
     }
     c->n_pending = 0;
+    return DOMINO_OK;
+}
+
+int domino_rollout_set_proposals(domino_ctx* c, int n) {
+    if (!c || n < 1 || n > kProposals) return DOMINO_ERR_INVALID_ARG;
+    c->n_proposals = n;
     return DOMINO_OK;
 }
 

@@ -172,6 +172,7 @@ struct domino_ctx {
     int device;
     int num_sms;
     int driver;
+    int n_proposals;  // early stop: proposals per block (1..15)
     int last_launches;
     bool loaded;
     // borrowed weights

@@ -30,6 +30,7 @@ struct RunArgs {
     const int32_t* verified;   // [B]
     int B;
     int K;                     // effective pool size: 0 = full vocabulary
+    int n_prop;                // proposals produced (1..15): p_1 + n_prop-1 corrected steps
     const int32_t* forced;     // nullable [B,15]
     domino_debug_bufs dbg;     // all-null when not debugging
     int32_t* out_tokens;       // [B,15]

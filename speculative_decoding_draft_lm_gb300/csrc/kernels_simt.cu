@@ -380,14 +380,15 @@ __global__ void __launch_bounds__(256) k_correct_pool(const T* __restrict__ fc2,
 
 // ---------------------------------------------------------------------------
 __global__ void k_finalize(const unsigned long long* __restrict__ keys, const int* __restrict__ bad,
-                           int32_t* __restrict__ out, float* __restrict__ dbg_top1, int B) {
+                           int32_t* __restrict__ out, float* __restrict__ dbg_top1, int B, int n_prop) {
     pdl_wait();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= B * kProposals) return;
     int b = i / kProposals, j = i % kProposals;
     unsigned long long key = keys[(size_t)b * kBlock + j];
-    out[i] = bad[b] ? -1 : (int32_t)key_index(key);
-    if (dbg_top1) dbg_top1[i] = key_value(key);
+    const bool used = j < n_prop;
+    out[i] = (bad[b] || !used) ? -1 : (int32_t)key_index(key);
+    if (dbg_top1) dbg_top1[i] = used ? key_value(key) : 0.f;
 }
 
 }  // namespace
@@ -497,7 +498,7 @@ cudaError_t launch_finalize(domino_ctx* c, RunArgs& r) {
     int n = r.B * kProposals;
     ++r.launches;
     return launch_pdl(k_finalize, dim3((n + 255) / 256), dim3(256), 0, r.st, (const unsigned long long*)c->keys,
-                      (const int*)c->bad, r.out_tokens, r.dbg.top1, r.B);
+                      (const int*)c->bad, r.out_tokens, r.dbg.top1, r.B, r.n_prop);
 }
 
 // The full-vocabulary correction kernel needs NB*F*4 bytes of dynamic shared

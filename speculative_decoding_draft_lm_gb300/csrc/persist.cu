@@ -57,6 +57,7 @@ struct PersistParams {
     float *dbg_h, *dbg_z, *dbg_scores;
     unsigned long long* trace;  // [grid][DOMINO_TRACE_SLOTS] or null
     int B, K, V, E, G, F, max_B;
+    int n_corr;     // corrected steps (early stop: fewer than 14)
     int seg;        // rows (K0) or pool entries per CTA
     int n_slots;
     int n_cons;     // consumer warps of the correction phase (divides n_slots)
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             // pool rows are re-read every step: keep them
             const uint64_t pol = full_vocab ? tc::policy_evict_normal() : tc::policy_evict_last();
             int q = 0;
-            for (int k = 1; k <= kCorrected && !*abort_flag; ++k) {
+            for (int k = 1; k <= p.n_corr && !*abort_flag; ++k) {
                 const bool fwd = (k & 1) != 0;
                 for (int ci = 0; ci < n_chunks; ++ci) {
                     const int c = fwd ? ci : n_chunks - 1 - ci;
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             if (lane == 0) atomicAdd((int*)consumed_ptr, 1);
         }
         // hidden-side GRU products for the next update while the ring refills
-        if (pre_gh && k < kCorrected && !*abort_flag) {
+        if (pre_gh && k < p.n_corr && !*abort_flag) {
             for (int it = warp; it < jn * 3; it += kConsumerWarps) {
                 const int jj = it / 3, gate = it % 3;
                 RegRow<T, NCH> wh;
@@ -711,7 +712,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         stamp();                                                     // 3
         if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
         stamp();                                                     // 4
-        for (int k = 1; k <= kCorrected; ++k) {                      // 5 + 6 (k-1) + ...
+        for (int k = 1; k <= p.n_corr; ++k) {                        // 5 + 6 (k-1) + ...
             prefetch_L(k);
             fc1(k);
             stamp();                                                 // +0 projector done
@@ -721,7 +722,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             stamp();                                                 // +2 correction done
             if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
             stamp();                                                 // +3 barrier
-            if (k < kCorrected) {
+            if (k < p.n_corr) {
                 gru(k + 1, pre_gh);
                 stamp();                                             // +4 GRU done
                 if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
@@ -829,6 +830,7 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     p.G = g.G;
     p.F = g.F;
     p.max_B = g.max_B;
+    p.n_corr = r.n_prop - 1;
     p.seg = seg;
     p.n_slots = n_slots;
     p.n_cons = n_cons;

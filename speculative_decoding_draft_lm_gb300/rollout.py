@@ -38,6 +38,7 @@ EXPORTED = (
     "domino_rollout_debug_run", "domino_rollout_set_driver", "domino_rollout_status",
     "domino_rollout_last_launch_count", "domino_rollout_destroy", "domino_rollout_strerror",
     "domino_rollout_enable_timing", "domino_rollout_read_timing", "domino_candidate_pool_static",
+    "domino_rollout_set_proposals",
 )
 
 PHASES = ("lmhead", "argmax", "pool", "gru", "fc1", "correct", "steps", "other")
@@ -89,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.domino_rollout_enable_timing.argtypes = [vp, i]
     lib.domino_rollout_read_timing.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
     lib.domino_candidate_pool_static.argtypes = [vp, i, i, i, vp, vp]
+    lib.domino_rollout_set_proposals.argtypes = [vp, i]
     lib.domino_rollout_strerror.argtypes = [i]
     lib.domino_rollout_strerror.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -150,6 +152,10 @@ def domino_rollout_debug_run(ctx, hidden, s, verified_tok, B: int, K: int, force
 
 def domino_rollout_set_driver(ctx, driver: int) -> int:
     return _check(load_library().domino_rollout_set_driver(ctx, driver), "domino_rollout_set_driver")
+
+
+def domino_rollout_set_proposals(ctx, n: int) -> int:
+    return _check(load_library().domino_rollout_set_proposals(ctx, n), "domino_rollout_set_proposals")
 
 
 def domino_rollout_status(ctx, stream=None) -> int:
@@ -224,6 +230,9 @@ class DominoRollout:
 
     def set_driver(self, driver: int):
         domino_rollout_set_driver(self.ctx, driver)
+
+    def set_proposals(self, n: int):
+        domino_rollout_set_proposals(self.ctx, n)
 
     def run(self, hidden, s, verified, K=0, out=None, stream=None):
         import torch

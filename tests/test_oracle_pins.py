@@ -256,3 +256,31 @@ def test_step_count_and_shapes():
     assert out["z"].shape == (2, 14, SMALL.F)
     assert out["c"][0].shape == (14, 40)
     assert all(len(p) == 40 and (np.diff(p) > 0).all() for p in out["pool"])
+
+
+@pytest.mark.parametrize("K", [0, 40])
+def test_early_stop_is_prefix_of_full_block(K):
+    """b8 keeps the block-16 draft and only verifies fewer positions: the n
+    proposals of an early-stopped rollout are the first n of the full one."""
+    w, r = _small(B=3)
+    full = oracle.run(w, r, K=K, keep_scores=True)
+    for n in (1, 2, 7, 14, 15):
+        part = oracle.run(w, r, K=K, keep_scores=True, n_proposals=n)
+        assert (part["tokens"][:, :n] == full["tokens"][:, :n]).all()
+        assert (part["tokens"][:, n:] == -1).all()
+        assert all((a == b).all() for a, b in zip(part["pool"], full["pool"]))
+        assert part["c"][0].shape == (n - 1, K if K else SMALL.V)
+        np.testing.assert_array_equal(part["z"][:, :n - 1], full["z"][:, :n - 1])
+        assert not part["z"][:, n - 1:].any()
+    with pytest.raises(ValueError):
+        oracle.run(w, r, n_proposals=0)
+    with pytest.raises(ValueError):
+        oracle.run(w, r, n_proposals=16)
+
+
+def test_early_stop_single_proposal_is_base_argmax():
+    w, r = _small(B=2)
+    out = oracle.run(w, r, n_proposals=1)
+    for b in range(2):
+        assert out["tokens"][b, 0] == int(np.argmax(out["L"][b, 1]))
+    assert (out["tokens"][:, 1:] == -1).all()
