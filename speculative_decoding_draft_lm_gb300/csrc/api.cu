@@ -117,8 +117,15 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         STEP(DOMINO_PHASE_STEPS, launch_persist(c, r));
     } else {
     const bool batch = r.B >= 2 && batch_kernels_supported(c);
-#define GRU(u) (batch ? launch_gru_batch(c, r, (u)) : launch_gru(c, r, (u)))
-#define FC1(k) (batch ? launch_fc1_batch(c, r, (k)) : launch_fc1(c, r, (k)))
+    // bf16 batches: GRU and projector layer 1 as tensor-core contractions
+    const bool gru_tc = batch && gru_tc_supported(c, r);
+    GruMaps gm;
+    if (gru_tc) {
+        e = prepare_gru_tc(c, r, &gm);
+        if (e != cudaSuccess) goto fail;
+    }
+#define GRU(u) (gru_tc ? launch_gru_tc(c, r, gm, (u)) : batch ? launch_gru_batch(c, r, (u)) : launch_gru(c, r, (u)))
+#define FC1(k) (gru_tc ? launch_fc1_tc(c, r, gm, (k)) : batch ? launch_fc1_batch(c, r, (k)) : launch_fc1(c, r, (k)))
     STEP(DOMINO_PHASE_GRU, GRU(0));
     STEP(DOMINO_PHASE_GRU, GRU(1));
     {
@@ -126,6 +133,7 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         // contraction (two or more requests); CUDA cores for B = 1 and pools
         const bool tc_corr = r.B >= 2 && correct_tc_supported(c, r);
         CUtensorMap tm_a;
+        if (tc_corr && r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_mask(c, r));
         if (tc_corr) {
             e = prepare_correct_tc(c, r, &tm_a);
             if (e != cudaSuccess) goto fail;
@@ -199,6 +207,12 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oBad = take((size_t)g.max_B * sizeof(int));
     size_t oErr = take(sizeof(int));
     size_t oSync = take(1024);
+    const bool gru_tc = gru_tc_shape_ok(g);
+    const size_t ldx = (size_t)g.E + g.G;
+    size_t oWp = take(gru_tc ? (size_t)4 * gru_padded_units(g.G) * ldx * 2 : 0);
+    size_t oX = take(gru_tc ? (size_t)2 * c->a_rows * ldx * 2 : 0);
+    const bool pmask = g.max_K > 0 && g.dtype == DOMINO_DTYPE_BF16;
+    size_t oM = take(pmask ? (size_t)g.max_B * pool_mask_words(g.V) * 4 : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -216,6 +230,9 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->bad = (int*)(base + oBad);
     c->err = (int*)(base + oErr);
     c->sync = (unsigned int*)(base + oSync);
+    c->wp = gru_tc ? (__nv_bfloat16*)(base + oWp) : nullptr;
+    c->xh16 = gru_tc ? (__nv_bfloat16*)(base + oX) : nullptr;
+    c->pmask = pmask ? (uint32_t*)(base + oM) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -248,6 +265,11 @@ int domino_rollout_load_weights(domino_ctx* c, const void* lm_head, const void* 
         const domino_config& g = c->cfg;
         if (make_tmap_bf16(&c->tm_lm_head, lm_head, (uint64_t)g.V, (uint64_t)g.H, 128) != cudaSuccess ||
             make_tmap_bf16(&c->tm_fc2, fc2, (uint64_t)g.V, (uint64_t)g.F, 128) != cudaSuccess) {
+            c->loaded = false;
+            return DOMINO_ERR_CUDA;
+        }
+        // the batched GRU contracts a packed copy of w_ih / w_hh (built here, once)
+        if (c->wp && (pack_gru_weights(c, 0) != cudaSuccess || cudaStreamSynchronize(0) != cudaSuccess)) {
             c->loaded = false;
             return DOMINO_ERR_CUDA;
         }

@@ -181,6 +181,7 @@ struct domino_ctx {
     float* L;                 // [max_B,16,V]
     float* score;             // [max_B,V]
     int32_t* pool;            // [max_B,max_K]
+    uint32_t* pmask;          // [max_B, ceil(V/32)] pool membership bits (bf16, max_K > 0), or null
     float* h;                 // [2][max_B,G] ping-pong
     float* a;                 // [max_B,F]
     __nv_bfloat16* a16;       // [a_rows,F] bf16 copy of a, zero padded
@@ -189,11 +190,14 @@ struct domino_ctx {
     int* bad;                 // [max_B] request saw an invalid token
     int* err;                 // device error word
     unsigned int* sync;       // grid-barrier words for the persistent driver
+    __nv_bfloat16* wp;        // [4*Gp, E+G] packed GRU weights (bf16 batches), or null
+    __nv_bfloat16* xh16;      // [2][a_rows, E+G] GRU operand rows [emb | bf16 h]
     void* ws_base;            // single workspace allocation
     size_t ws_bytes;
     // TMA descriptors (bf16 path)
     CUtensorMap tm_lm_head;
     CUtensorMap tm_fc2;
+    CUtensorMap tm_wp;
     bool has_tma;
     // per-phase timing (host side)
     bool timing;

@@ -10,6 +10,13 @@
 // base_logits full-vocabulary argmax) and page "Add correctness-first Domino
 // support to DFlash V2", section "Design" (full-vocabulary correction, K=0).
 // The activations are rounded to bf16 for the MMA; accumulation is fp32.
+//
+// Pool mode at large B*K (page "Add correctness-first Domino support to
+// DFlash V2", section "Design": block-shared top-K candidate pool): when the
+// pools of the batch together cover a large part of the vocabulary, gathering
+// B*K fc2 rows costs about as much as streaming fc2 once, so the same dense
+// contraction runs and the argmax only admits each request's pool members
+// (a [B, V/32] bit mask built from the pool).  The result is the pool argmax.
 #include "gemm_tc.cuh"
 #include "internal.h"
 
@@ -18,17 +25,19 @@ namespace domino {
 namespace {
 
 struct EpiCorrect {
+    static constexpr int kScratchWords = tc::kEpiScratch;
     const __nv_bfloat16* bias;  // [V]
     const float* L;             // [B,16,V]
     unsigned long long* keys;   // [B,16]
-    float* dbg_scores;          // [B,14,V] or null
-    int V, B, k;
+    float* dbg_scores;          // [B,14,V] or null (never with a mask)
+    const uint32_t* mask;       // [B, mask_words] pool membership bits, or null = full vocabulary
+    int V, B, k, mask_words;
     __device__ __forceinline__ void begin(unsigned long long* sb, int t) const {
-        for (int i = t; i < tc::kEpiScratch; i += 128) sb[i] = 0ull;
+        for (int i = t; i < tc::kEpiScratch; i += tc::kEpiThreads) sb[i] = 0ull;
     }
     __device__ __forceinline__ void end(unsigned long long* sb, int t) const {
         const int n = B < tc::kEpiScratch ? B : tc::kEpiScratch;
-        for (int b = t; b < n; b += 128)
+        for (int b = t; b < n; b += tc::kEpiThreads)
             if (sb[b]) atomicMax(&keys[(size_t)b * kBlock + k], sb[b]);
     }
     // base logits of the tile's first PF requests for this thread's row
@@ -54,11 +63,19 @@ struct EpiCorrect {
                 base[j] = (ok && j < nb) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
         }
         const float bv = ok ? __bfloat162float(bias[row]) : 0.f;
+        uint32_t member = 0xffffu;  // bit j: column j may take this row
+        if (mask && ok) {
+            member = 0u;
+            const uint32_t* mw = mask + (size_t)col0 * mask_words + (row >> 5);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (j < nb) member |= ((__ldg(mw + (size_t)j * mask_words) >> (row & 31)) & 1u) << j;
+        }
         unsigned long long kk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             kk[j] = 0ull;
-            if (ok && j < nb) {
+            if (ok && j < nb && ((member >> j) & 1u)) {
                 const float c = v[j] + bv + base[j];
                 kk[j] = pack_key(c, (uint32_t)row);
                 if (dbg_scores) dbg_scores[((size_t)(col0 + j) * kCorrected + (k - 1)) * V + row] = c;
@@ -77,7 +94,7 @@ struct EpiCorrect {
 
 template <int BN>
 cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) {
-    using S = tc::GemmShape<BN>;
+    using S = tc::GemmShape<BN, EpiCorrect::kScratchWords>;
     static bool attr_set[64] = {};
     auto kern = tc::k_gemm_tc<BN, EpiCorrect>;
     const int slot = c->device & 63;
@@ -88,7 +105,9 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) 
     }
     const int tiles = ((c->cfg.V + tc::kBM - 1) / tc::kBM) * ((r.B + BN - 1) / BN);
     const int grid = tiles < c->num_sms ? tiles : c->num_sms;
-    EpiCorrect epi{(const __nv_bfloat16*)c->bias, c->L, c->keys, r.dbg.scores, c->cfg.V, r.B, k};
+    const bool pool = r.K > 0;
+    EpiCorrect epi{(const __nv_bfloat16*)c->bias, c->L, c->keys, pool ? nullptr : r.dbg.scores,
+                   pool ? c->pmask : nullptr, c->cfg.V, r.B, k, pool_mask_words(c->cfg.V)};
     ++r.launches;
     return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_fc2, tmB, c->cfg.V, r.B,
                       c->cfg.F, epi, c->err);
@@ -98,8 +117,39 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) 
 
 int correct_bn(int B) { return B <= 16 ? 16 : B <= 32 ? 32 : B <= 64 ? 64 : B <= 128 ? 128 : 256; }
 
+int pool_mask_words(int V) { return (V + 31) / 32; }
+
 bool correct_tc_supported(const domino_ctx* c, const RunArgs& r) {
-    return c->has_tma && c->cfg.dtype == DOMINO_DTYPE_BF16 && r.K == 0 && r.B <= c->a_rows;
+    if (!c->has_tma || c->cfg.dtype != DOMINO_DTYPE_BF16 || r.B > c->a_rows) return false;
+    if (r.K == 0) return true;
+    // pools covering at least half a vocabulary's worth of rows between them;
+    // score dumps keep the gathering path (they are indexed by pool position)
+    return c->pmask != nullptr && 2LL * r.B * r.K >= (long long)c->cfg.V && r.dbg.scores == nullptr;
+}
+
+namespace {
+
+__global__ void __launch_bounds__(256) k_pool_mask(const int32_t* __restrict__ pool, uint32_t* __restrict__ mask,
+                                                   int K, int words) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x;
+    uint32_t* m = mask + (size_t)b * words;
+    for (int i = threadIdx.x; i < words; i += blockDim.x) m[i] = 0u;
+    __syncthreads();
+    const int32_t* p = pool + (size_t)b * K;
+    for (int i = threadIdx.x; i < K; i += blockDim.x) {
+        const int v = p[i];
+        atomicOr(&m[v >> 5], 1u << (v & 31));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pool_mask(domino_ctx* c, RunArgs& r) {
+    ++r.launches;
+    return launch_pdl(k_pool_mask, dim3(r.B), dim3(256), 0, r.st, (const int32_t*)c->pool, c->pmask, r.K,
+                      pool_mask_words(c->cfg.V));
 }
 
 cudaError_t prepare_correct_tc(domino_ctx* c, RunArgs& r, CUtensorMap* tmB) {

@@ -6,13 +6,18 @@
 //   warp 1      TMEM allocator + MMA issuer (one thread): 4 x tcgen05.mma
 //               (M=128, N=BN, K=16) per k-chunk into one of two TMEM
 //               accumulators, tcgen05.commit frees the ring slot
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               row of A), handed to the Epi functor 16 columns at a time
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               row of A), handed to the Epi functor 16 columns at a time;
+//               warp w reads TMEM lanes 32*(w%4).., warps 2..5 take the first
+//               half of the tile's 16-column chunks and warps 6..9 the second,
+//               so that a wide tile's epilogue keeps pace with its MMAs
 //
 // Epi provides begin(scratch, t) / prefetch(col0, row, pf) /
 // operator()(col0, row, v[16], lane, scratch, pf + 16c) / end(scratch, t),
-// t = epilogue thread 0..127; `scratch` is kEpiScratch per-block 64-bit words
-// (per-request argmax words) in shared memory; `pf` holds up to kPrefetch
+// t = epilogue thread 0..kEpiThreads-1; `scratch` is Epi::kScratchWords per-block
+// 64-bit words in shared memory (per-request argmax words); operator() must
+// not wait on the other epilogue warps (after a timed-out wait they may have
+// left the tile loop); `pf` holds up to kPrefetch
 // values per thread that the epilogue may load for the next tile while the
 // MMAs of that tile are still running.
 //
@@ -30,27 +35,29 @@ namespace tc {
 
 constexpr int kBM = 128;          // rows of A per tile (MMA M)
 constexpr int kBK = 64;           // K elements per chunk (128 bytes of bf16)
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kGemmThreads = 64 + kEpiThreads;
 constexpr int kEpiScratch = 256;  // 64-bit words
 constexpr int kPrefetch = 64;     // per-thread epilogue prefetch registers
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
 
-template <int BN>
+template <int BN, int SCRATCH_WORDS = kEpiScratch>
 struct GemmShape {
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN * kBK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = (196608 / STAGE) > 12 ? 12 : (196608 / STAGE);
     static constexpr int TMEM_COLS = (2 * BN) < 32 ? 32 : 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 512 + 8 * kEpiScratch;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 + 512 + 8 * SCRATCH_WORDS;
 };
 
 template <int BN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
               int K, Epi epi, int* err) {
-    using S = GemmShape<BN>;
+    using S = GemmShape<BN, Epi::kScratchWords>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S::STAGES * S::STAGE);
@@ -71,7 +78,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, 128);
+            mbar_init(tempty0 + 8 * b, kEpiThreads);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -175,15 +182,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         const int quarter = warp & 3;
         const int et = threadIdx.x - 64;
+        // chunks [c_lo, c_hi) of every tile belong to this half of the epilogue warps
+        constexpr int NC = BN / 16, HC = (NC + 1) / 2;
+        const int half = et / 128;
+        const int c_lo = half * HC, c_hi = (half + 1) * HC < NC ? (half + 1) * HC : NC;
         int acc = 0;
         uint32_t acc_phase = 0;
         epi.begin(scratch, et);
         epi_bar();
-        constexpr int PF = BN < kPrefetch ? BN : kPrefetch;
+        constexpr int PF = 16 * HC < kPrefetch ? 16 * HC : kPrefetch;
         float pf[PF];
-        if ((int)blockIdx.x < tiles) {
+        if ((int)blockIdx.x < tiles && c_lo < c_hi) {
             const int t0 = blockIdx.x;
-            epi.template prefetch<PF>((t0 % n_tiles) * BN, (t0 / n_tiles) * kBM + quarter * 32 + lane, pf);
+            epi.template prefetch<PF>((t0 % n_tiles) * BN + 16 * c_lo, (t0 / n_tiles) * kBM + quarter * 32 + lane, pf);
         }
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) break;
@@ -192,14 +203,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int row = m * kBM + quarter * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll
-            for (int c = 0; c < BN / 16; ++c) {
-                float v[16];
-                tmem_ld16(tbase + 16 * c, v);
-                epi(n * BN + 16 * c, row, v, lane, scratch, 16 * c < PF ? pf + 16 * c : nullptr);
+            for (int i = 0; i < HC; ++i) {
+                const int c = c_lo + i;
+                if (c < c_hi) {  // uniform over the warp
+                    float v[16];
+                    tmem_ld16(tbase + 16 * c, v);
+                    epi(n * BN + 16 * c, row, v, lane, scratch, 16 * i < PF ? pf + 16 * i : nullptr);
+                }
             }
             const int tn = t + gridDim.x;  // the next tile's epilogue inputs, during its MMAs
-            if (tn < tiles)
-                epi.template prefetch<PF>((tn % n_tiles) * BN, (tn / n_tiles) * kBM + quarter * 32 + lane, pf);
+            if (tn < tiles && c_lo < c_hi)
+                epi.template prefetch<PF>((tn % n_tiles) * BN + 16 * c_lo, (tn / n_tiles) * kBM + quarter * 32 + lane,
+                                          pf);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
             if (++acc == 2) {

@@ -53,12 +53,18 @@ cudaError_t prepare_simt_kernels(domino_ctx* c);
 
 // tcgen05 / TMA kernels (lmhead_tc.cu)
 cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+cudaError_t make_tmap_bf16_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                                   uint32_t box_rows);
 bool lmhead_tc_supported(const domino_ctx* c);
 // also writes p_1's argmax word and, when r.K > 0, the pool scores
 cudaError_t launch_lmhead_tc(domino_ctx* c, RunArgs& r);
 
 // tcgen05 correction over the full vocabulary (correct_tc.cu)
+int correct_bn(int B);  // N tile of the batched tensor-core kernels
+int pool_mask_words(int V);
+// full vocabulary, or (with a pool membership mask) pools that cover much of it
 bool correct_tc_supported(const domino_ctx* c, const RunArgs& r);
+cudaError_t launch_pool_mask(domino_ctx* c, RunArgs& r);  // after the pool selection
 cudaError_t prepare_correct_tc(domino_ctx* c, RunArgs& r, CUtensorMap* tmB);
 cudaError_t launch_correct_tc(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k);
 
@@ -74,6 +80,20 @@ cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u);
 cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k);
 bool pool_batch_supported(const domino_ctx* c);
 cudaError_t launch_correct_pool_batch(domino_ctx* c, RunArgs& r, int k);
+
+// tcgen05 GRU update and projector layer 1 for B >= 2 (gru_tc.cu)
+struct GruMaps {
+    CUtensorMap x[2];  // operand rows [emb | bf16 h] of X[0], X[1]
+    CUtensorMap h[2];  // the state columns of X[0], X[1]
+    CUtensorMap fc1;
+};
+int gru_padded_units(int G);
+bool gru_tc_shape_ok(const domino_config& g);
+bool gru_tc_supported(const domino_ctx* c, const RunArgs& r);
+cudaError_t pack_gru_weights(domino_ctx* c, cudaStream_t st);
+cudaError_t prepare_gru_tc(domino_ctx* c, RunArgs& r, GruMaps* m);
+cudaError_t launch_gru_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int u);
+cudaError_t launch_fc1_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int k);
 
 // persistent driver of the GRU seed and the 14 corrected steps (persist.cu)
 bool persist_supported(const domino_ctx* c, const RunArgs& r);

@@ -21,16 +21,17 @@ namespace domino {
 namespace {
 
 struct EpiLmHead {
+    static constexpr int kScratchWords = tc::kEpiScratch;
     float* L;                  // [B,16,V]
     unsigned long long* keys;  // [B,16], slot 0 = p_1
     float* score;              // [B,V] or null
     int V, B;
     __device__ __forceinline__ void begin(unsigned long long* sb, int t) const {
-        for (int i = t; i < tc::kEpiScratch; i += 128) sb[i] = 0ull;
+        for (int i = t; i < tc::kEpiScratch; i += tc::kEpiThreads) sb[i] = 0ull;
     }
     __device__ __forceinline__ void end(unsigned long long* sb, int t) const {
         const int n = B < tc::kEpiScratch ? B : tc::kEpiScratch;
-        for (int b = t; b < n; b += 128)
+        for (int b = t; b < n; b += tc::kEpiThreads)
             if (sb[b]) atomicMax(&keys[(size_t)b * kBlock], sb[b]);
     }
     template <int PF>
@@ -75,7 +76,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 template <int BN>
 cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, float* score) {
-    using S = tc::GemmShape<BN>;
+    using S = tc::GemmShape<BN, EpiLmHead::kScratchWords>;
     static bool attr_set[64] = {};
     auto kern = tc::k_gemm_tc<BN, EpiLmHead>;
     const int slot = c->device & 63;
@@ -95,19 +96,25 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, float* 
 
 }  // namespace
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box {64, box_rows},
-// 128-byte swizzle, zero fill outside the matrix.
-cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix whose rows are
+// `ld` elements apart, box {64, box_rows}, 128-byte swizzle, zero fill
+// outside the matrix.
+cudaError_t make_tmap_bf16_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                                   uint32_t box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {ld * 2};
     cuuint32_t box[2] = {(cuuint32_t)tc::kBK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    return make_tmap_bf16_strided(m, base, rows, cols, cols, box_rows);
 }
 
 bool lmhead_tc_supported(const domino_ctx* c) { return c->has_tma && c->cfg.dtype == DOMINO_DTYPE_BF16; }

@@ -86,6 +86,14 @@ def test_hand_worked_golden_on_gpu():
 
 # ---- full-size workloads ---------------------------------------------------
 
+@pytest.mark.parametrize("K", [0, 100])
+@pytest.mark.parametrize("B", [16, 37])
+def test_small_batches_on_the_tensor_core_gru(B, K):
+    """B >= 12: GRU and projector layer 1 run as tcgen05 contractions."""
+    sh = inputs.small_shape(dtype="bf16")
+    _parity(sh, B, K, seeds=list(range(200, 200 + B)), scales=FEEDBACK_SCALES(sh))
+
+
 @pytest.mark.parametrize("name", ["qwen3_8b_b1_k0", "qwen3_8b_b8_k0", "qwen3_8b_b64_k0",
                                   "qwen3_8b_b1_k2048", "qwen3_8b_b8_k2048", "qwen3_8b_b64_k2048",
                                   "large_b64_k0", "large_b64_k2048"])
