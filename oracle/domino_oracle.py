@@ -19,6 +19,7 @@ speculative decoding (V2)", section "Implementation"):
      p_{k+1}= argmax_v c[v]
      if k < 14: h = GRU(emb[p_{k+1}], h)            feedback update
   rho(j)    = j + 1
+  s[j]      = W_hid . X[rho(j)]  when s is not given (backbone half of layer 1)
 
 Readings taken where the pages are silent (each is listed in the design notes
 of the repository): rho(j) = j + 1 (block position 0 is the verified token);
@@ -140,14 +141,34 @@ class OracleWeights:
         self.F = self.fc1.shape[0]
 
 
+def backbone_s(hidden, W_hid) -> np.ndarray:
+    """Per-step additive term of projector layer 1 from the backbone hidden.
+
+    The projector's first layer acts on the concatenation [backbone hidden |
+    GRU state] (page "Add correctness-first Domino support to DFlash V2",
+    the "add Domino drafter training backend" change: a low-rank embed_proj
+    over [backbone hidden | GRU state]), so with W1 = [W_hid | fc1] it splits
+    into W_hid . hidden + fc1 . h.  The term for proposal j uses the hidden
+    state of the block row whose base logits that proposal corrects,
+    rho(j) = j + 1.  Returns s [B, 15, F]:
+
+        s[b, j, f] = sum_h hidden[b, rho(j), h] * W_hid[f, h]
+    """
+    X = widen(hidden)[:, ROW_OFFSET:ROW_OFFSET + N_PROPOSALS]   # [B,15,H]
+    return np.einsum("bjh,fh->bjf", X, widen(W_hid))
+
+
 def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
-            keep_scores: bool = False, n_proposals: int = N_PROPOSALS) -> dict:
+            keep_scores: bool = False, n_proposals: int = N_PROPOSALS, W_hid=None) -> dict:
     """Run the Domino rollout for a batch of independent requests.
 
     ``hidden`` [B,16,H], ``s`` [B,15,F], ``verified`` [B] int.  ``forced``
     (optional [B,15] ints) teacher-forces the chain: the GRU is fed
     ``forced[:, k]`` instead of the rollout's own choice, while the rollout's
     own argmax is still reported in ``tokens``.
+
+    ``s`` may be None when ``W_hid`` ([F, H], the backbone-hidden half of
+    projector layer 1) is given: then s = backbone_s(hidden, W_hid).
 
     ``n_proposals`` (1..15) stops the chain after that many proposals, as
     for a target that verifies only the first n+1 block positions (page
@@ -169,7 +190,12 @@ def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
     n_corr = n_proposals - 1
     B = hidden.shape[0]
     L = lm_head(hidden, W.lm_head)                     # [B,16,V]
-    s64 = widen(s)
+    if s is None:
+        if W_hid is None:
+            raise ValueError("either s or W_hid is needed")
+        s64 = backbone_s(hidden, W_hid)
+    else:
+        s64 = widen(s)
     tokens = np.zeros((B, N_PROPOSALS), dtype=np.int64)
     margin = np.zeros((B, N_PROPOSALS))
     top1 = np.zeros((B, N_PROPOSALS))
@@ -231,5 +257,5 @@ def rollout(W: OracleWeights, hidden, s, verified, K: int = 0, forced=None,
 
 def run(weights: dict, requests: dict, K: int = 0, **kw) -> dict:
     """Convenience wrapper: widen ``weights`` and run ``rollout``."""
-    return rollout(OracleWeights(weights), requests["hidden"], requests["s"],
+    return rollout(OracleWeights(weights), requests["hidden"], requests.get("s"),
                    requests["verified"], K, **kw)

@@ -124,6 +124,13 @@ def make_weights(sh: Shape, seed: int = 0, scales: dict | None = None) -> dict:
     return {n: _normal(gen, shapes[n], scales.get(n, 0.02), sh.dtype) for n in WEIGHT_NAMES}
 
 
+def make_fc1_hidden(sh: Shape, seed: int = 0, scale: float = 0.02) -> np.ndarray:
+    """Backbone-hidden half of projector layer 1, [F, H] (its own stream, so
+    the other weights do not change when it is drawn)."""
+    gen = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(2,))))
+    return _normal(gen, (sh.F, sh.H), scale, sh.dtype)
+
+
 def make_requests(sh: Shape, request_seeds) -> dict:
     """Per-request draft hidden states, per-step ``s`` rows and verified tokens."""
     B = len(request_seeds)

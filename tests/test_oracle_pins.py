@@ -284,3 +284,33 @@ def test_early_stop_single_proposal_is_base_argmax():
     for b in range(2):
         assert out["tokens"][b, 0] == int(np.argmax(out["L"][b, 1]))
     assert (out["tokens"][:, 1:] == -1).all()
+
+
+def test_backbone_s_is_the_hidden_half_of_one_linear_layer():
+    """z = W1 [hidden(rho(k)) | h] with W1 = [W_hid | fc1], one torch Linear."""
+    torch = pytest.importorskip("torch")
+    w, r = _small(B=2)
+    W_hid = inputs.make_fc1_hidden(SMALL, seed=3, scale=0.1)
+    out = oracle.rollout(oracle.OracleWeights(w), r["hidden"], None, r["verified"], 0, W_hid=W_hid)
+    W1 = torch.from_numpy(np.concatenate([np.asarray(W_hid, np.float64), np.asarray(w["fc1"], np.float64)], axis=1))
+    for b in range(2):
+        for k in range(1, 15):
+            x = np.concatenate([np.asarray(r["hidden"][b, k + 1], np.float64), out["h"][b, k]])
+            z = torch.nn.functional.linear(torch.from_numpy(x), W1).numpy()
+            np.testing.assert_allclose(out["z"][b, k - 1], z, rtol=0, atol=1e-10)
+
+
+def test_backbone_s_matches_explicit_s_and_brute_force():
+    w, r = _small(B=2)
+    W_hid = inputs.make_fc1_hidden(SMALL, seed=3, scale=0.1)
+    s = oracle.backbone_s(r["hidden"], W_hid)
+    # brute force for a few entries
+    for b, j, f in [(0, 0, 0), (1, 14, 19), (0, 7, 11)]:
+        want = sum(float(r["hidden"][b, j + 1, h]) * float(W_hid[f, h]) for h in range(SMALL.H))
+        assert abs(s[b, j, f] - want) < 1e-9
+    a = oracle.rollout(oracle.OracleWeights(w), r["hidden"], s, r["verified"], 40)
+    c = oracle.rollout(oracle.OracleWeights(w), r["hidden"], None, r["verified"], 40, W_hid=W_hid)
+    assert (a["tokens"] == c["tokens"]).all()
+    np.testing.assert_array_equal(a["z"], c["z"])
+    with pytest.raises(ValueError):
+        oracle.rollout(oracle.OracleWeights(w), r["hidden"], None, r["verified"], 0)
