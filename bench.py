@@ -63,13 +63,18 @@ def load_peaks():
 
 # ---- algorithmic bytes / flops -------------------------------------------
 
-def alg_bytes(sh: inputs.Shape, B: int, K: int, n_prop: int = 15) -> dict:
+def alg_bytes(sh: inputs.Shape, B: int, K: int, n_prop: int = 15, s_in_library: bool = False) -> dict:
     """Algorithmic bytes per launch of each phase and per block; ``n_prop``
-    proposals take max(2, n_prop) GRU updates and n_prop - 1 corrected steps."""
+    proposals take max(2, n_prop) GRU updates and n_prop - 1 corrected steps;
+    ``s_in_library`` adds W_hid and the s rows to the LM-head launch."""
     e = 2 if sh.dtype == "bf16" else 4
     V, H, E, G, F = sh.V, sh.H, sh.E, sh.G, sh.F
     full = K == 0 or K >= V
     lm = V * H * e + B * 16 * H * e + B * 16 * V * 4
+    lm_flop = 2.0 * B * 16 * V * H
+    if s_in_library:
+        lm += F * H * e + B * 15 * F * e
+        lm_flop += 2.0 * B * 16 * F * H
     if full:
         corr = V * F * e + V * e + B * V * 4 + B * F * 4
     else:
@@ -81,7 +86,7 @@ def alg_bytes(sh: inputs.Shape, B: int, K: int, n_prop: int = 15) -> dict:
     steps = max(2, n_prop) * gru + (n_prop - 1) * (fc1 + corr)
     per_block = lm + pool + steps
     return {"lmhead": lm, "correct": corr, "gru": gru, "fc1": fc1, "pool": pool, "steps": steps,
-            "block": per_block, "lmhead_flop": 2.0 * B * 16 * V * H}
+            "block": per_block, "lmhead_flop": lm_flop}
 
 
 # ---- clocks sampler ---------------------------------------------------------
@@ -494,14 +499,22 @@ def main():
                         "note": "A100 numbers at the pages' checkpoint shapes; context only"}}
 
     # B = 1/8/64 x K0/K2048 table on the same weights (rank 0), then the
-    # early-stopped b8 variant (7 proposals) of the B = 1/8 workloads
+    # early-stopped b8 variant (7 proposals) of the B = 1/8 workloads, then
+    # K0 with s derived in the library from the backbone hidden rows
     if sweep:
         table = {}
-        for name, n_prop in [(n, 15) for n in sweep] + [(n, 7) for n in sweep if inputs.WORKLOADS[n].B <= 8]:
+        runs = ([(n, 15, False) for n in sweep] + [(n, 7, False) for n in sweep if inputs.WORKLOADS[n].B <= 8] +
+                [(n, 15, True) for n in sweep if inputs.WORKLOADS[n].K == 0])
+        if any(r_[2] for r_ in runs):
+            w_hid = to_device(inputs.make_fc1_hidden(sh, seed=5))
+            eng.load_backbone_proj(w_hid)
+        for name, n_prop, own_s in runs:
             w2 = inputs.WORKLOADS[name]
             eng.set_proposals(n_prop)
             rq = inputs.make_requests(sh, list(w2.request_seeds))
             h2, s2, v2 = to_device(rq["hidden"]), to_device(rq["s"]), torch.from_numpy(rq["verified"]).cuda()
+            if own_s:
+                s2 = None
             for _ in range(3):
                 step(h2, s2, v2, w2.B, w2.K)
             n_sweep = max(5, args.steps // 2)
@@ -534,10 +547,11 @@ def main():
                         ph_ms[k_] = ph_ms.get(k_, 0.0) + m_
             eng.enable_timing(False)
             ms = sum(tt) / len(tt)
-            ab2 = alg_bytes(sh, w2.B, w2.K, n_prop)
+            ab2 = alg_bytes(sh, w2.B, w2.K, n_prop, own_s)
             lm_avg = lm_ms / max(1, lm_n)
-            table[name if n_prop == 15 else f"{name}_n{n_prop}"] = {
-                "us_per_block": ms * 1e3, "proposals": n_prop,
+            label = name + ("" if n_prop == 15 else f"_n{n_prop}") + ("_s_in_library" if own_s else "")
+            table[label] = {
+                "us_per_block": ms * 1e3, "proposals": n_prop, "s": "in library" if own_s else "input",
                 "proposals_per_s": float(n_prop) * w2.B / (ms * 1e-3),
                 "hbm_frac_block": ab2["block"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "lmhead_us": lm_avg * 1e3,

@@ -89,11 +89,26 @@ DOMINO_API int domino_rollout_load_weights(domino_ctx* ctx, const void* lm_head,
                                 const void* w_ih, const void* w_hh, const void* fc1,
                                 const void* fc2, const void* bias);
 
+/* Optional: the backbone-hidden half W_hid [F,H] of projector layer 1, a
+ * DEVICE pointer in the config dtype, row-major, 16-byte aligned, BORROWED
+ * like the other weights (NULL unregisters it).  The projector's first layer
+ * acts on [backbone hidden | GRU state] (page "Add correctness-first Domino
+ * support to DFlash V2", the Domino drafter training backend change), so its
+ * per-step term is s[b,j,:] = W_hid . hidden[b,j+1,:]: the hidden row whose
+ * base logits proposal j corrects.  With it registered, run/debug_run accept
+ * s == NULL and compute s in the library (bf16: as extra rows of the LM-head
+ * contraction, stored as bf16; fp32: on the CUDA cores).  No bias is added.
+ * Errors: INVALID_ARG. */
+DOMINO_API int domino_rollout_load_backbone_proj(domino_ctx* ctx, const void* w_hid);
+
 /* Run one block rollout for B requests on `cuda_stream` (a cudaStream_t,
  * NULL = legacy default stream).  DEVICE pointers, owned by the caller:
  *   hidden       [B,16,H]  draft hidden states (config dtype, 16-B aligned)
  *   s            [B,15,F]  per-step additive term of projector layer 1
- *                          (row 0 is not read; row k serves corrected step k)
+ *                          (row 0 is not read; row k serves corrected step k);
+ *                          NULL = compute it from `hidden` with the weight given
+ *                          to domino_rollout_load_backbone_proj (INVALID_ARG if
+ *                          none was given)
  *   verified_tok [B] int32 the block's verified token
  *   out_tokens   [B,15] int32 proposals p_1..p_15 (written)
  * K: pool size; 0 (or >= V) = full-vocabulary correction; 0 < K < V needs

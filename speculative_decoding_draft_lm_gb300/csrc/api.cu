@@ -65,16 +65,19 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         c->last_launches = 0;
         return DOMINO_OK;
     }
-    if (!hidden || !s || !verified || !out) return DOMINO_ERR_INVALID_ARG;
+    // s == null: derive it from the hidden rows with the loaded W_hid
+    if (!hidden || !verified || !out || (!s && !c->fc1_hid)) return DOMINO_ERR_INVALID_ARG;
     const int Keff = (K >= c->cfg.V) ? 0 : K;
     if (Keff > c->cfg.max_K) return DOMINO_ERR_INVALID_ARG;
-    if (c->cfg.dtype == DOMINO_DTYPE_BF16 && (!aligned16(hidden) || !aligned16(s))) return DOMINO_ERR_INVALID_ARG;
+    if (c->cfg.dtype == DOMINO_DTYPE_BF16 && (!aligned16(hidden) || (s && !aligned16(s))))
+        return DOMINO_ERR_INVALID_ARG;
 
     DeviceGuard guard(c->device);
     RunArgs r;
     memset(&r, 0, sizeof(r));
     r.hidden = hidden;
-    r.s = s;
+    r.s = s ? s : c->s_ws;
+    r.s_out = s ? nullptr : c->s_ws;
     r.verified = verified;
     r.B = B;
     r.K = Keff;
@@ -104,11 +107,12 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     } while (0)
     STEP(DOMINO_PHASE_OTHER, launch_reset(c, r));
     {
-        const bool tc_path = lmhead_tc_supported(c);
+        const bool tc_path = lmhead_tc_supported(c) && (!r.s_out || c->has_fc1h_tmap);
         if (tc_path) {
-            STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_tc(c, r));
+            STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_tc(c, r));  // s rides along when r.s_out is set
         } else {
             STEP(DOMINO_PHASE_LMHEAD, launch_lmhead_simt(c, r));
+            if (r.s_out) STEP(DOMINO_PHASE_LMHEAD, launch_backbone_s_simt(c, r));
             STEP(DOMINO_PHASE_ARGMAX, launch_first_argmax(c, r));
         }
         if (r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, tc_path));
@@ -200,6 +204,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oL = take((size_t)g.max_B * kBlock * g.V * sizeof(float));
     size_t oS = take(g.max_K > 0 ? (size_t)g.max_B * g.V * sizeof(float) : 0);
     size_t oP = take((size_t)g.max_B * (g.max_K > 0 ? g.max_K : 1) * sizeof(int32_t));
+    size_t oSw = take((size_t)g.max_B * kProposals * g.F * (g.dtype == DOMINO_DTYPE_BF16 ? 2 : 4));
     size_t oH = take((size_t)2 * g.max_B * g.G * sizeof(float));
     size_t oA = take((size_t)g.max_B * g.F * sizeof(float));
     size_t oA16 = take((size_t)c->a_rows * g.F * sizeof(__nv_bfloat16));
@@ -223,6 +228,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->L = (float*)(base + oL);
     c->score = (float*)(base + oS);
     c->pool = (int32_t*)(base + oP);
+    c->s_ws = base + oSw;
     c->h = (float*)(base + oH);
     c->a = (float*)(base + oA);
     c->a16 = (__nv_bfloat16*)(base + oA16);
@@ -276,6 +282,26 @@ int domino_rollout_load_weights(domino_ctx* c, const void* lm_head, const void* 
         c->has_tma = true;
     }
     c->loaded = true;
+    return DOMINO_OK;
+}
+
+int domino_rollout_load_backbone_proj(domino_ctx* c, const void* w_hid) {
+    if (!c) return DOMINO_ERR_INVALID_ARG;
+    if (!w_hid) {
+        c->fc1_hid = nullptr;
+        c->has_fc1h_tmap = false;
+        return DOMINO_OK;
+    }
+    if (!aligned16(w_hid)) return DOMINO_ERR_INVALID_ARG;
+    c->fc1_hid = w_hid;
+    c->has_fc1h_tmap = false;
+    if (c->cfg.dtype == DOMINO_DTYPE_BF16) {
+        DeviceGuard guard(c->device);
+        // 16-byte TMA row stride; otherwise the CUDA-core path computes s
+        if (c->cfg.H % 8 == 0 &&
+            make_tmap_bf16(&c->tm_fc1h, w_hid, (uint64_t)c->cfg.F, (uint64_t)c->cfg.H, 128) == cudaSuccess)
+            c->has_fc1h_tmap = true;
+    }
     return DOMINO_OK;
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
+
 #include "domino_rollout.h"
 
 namespace domino {
@@ -177,10 +179,12 @@ struct domino_ctx {
     bool loaded;
     // borrowed weights
     const void *lm_head, *emb, *w_ih, *w_hh, *fc1, *fc2, *bias;
+    const void* fc1_hid;      // [F,H] backbone-hidden half of projector layer 1, or null
     // workspace (owned)
     float* L;                 // [max_B,16,V]
     float* score;             // [max_B,V]
     int32_t* pool;            // [max_B,max_K]
+    void* s_ws;               // [max_B,15,F] input dtype: s computed from the backbone hidden
     uint32_t* pmask;          // [max_B, ceil(V/32)] pool membership bits (bf16, max_K > 0), or null
     float* h;                 // [2][max_B,G] ping-pong
     float* a;                 // [max_B,F]
@@ -198,6 +202,8 @@ struct domino_ctx {
     CUtensorMap tm_lm_head;
     CUtensorMap tm_fc2;
     CUtensorMap tm_wp;
+    CUtensorMap tm_fc1h;
+    bool has_fc1h_tmap;
     bool has_tma;
     // per-phase timing (host side)
     bool timing;

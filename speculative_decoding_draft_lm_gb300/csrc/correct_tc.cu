@@ -109,8 +109,8 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, int k) 
     EpiCorrect epi{(const __nv_bfloat16*)c->bias, c->L, c->keys, pool ? nullptr : r.dbg.scores,
                    pool ? c->pmask : nullptr, c->cfg.V, r.B, k, pool_mask_words(c->cfg.V)};
     ++r.launches;
-    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_fc2, tmB, c->cfg.V, r.B,
-                      c->cfg.F, epi, c->err);
+    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_fc2, c->tm_fc2, tmB, c->cfg.V,
+                      INT_MAX, r.B, c->cfg.F, epi, c->err);
 }
 
 }  // namespace

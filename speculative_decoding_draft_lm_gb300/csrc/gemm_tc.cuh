@@ -21,6 +21,11 @@
 // values per thread that the epilogue may load for the next tile while the
 // MMAs of that tile are still running.
 //
+// A second A matrix may follow the first: tiles m >= m_split read their 128
+// rows from tmA2 at row (m - m_split) * 128, so that two weight matrices that
+// share the B operand run in one launch (the epilogue sees the virtual row
+// m * 128 + r).
+//
 // Tiles are visited m-major (tile t -> m = t / n_tiles, n = t % n_tiles), grid
 // stride over a persistent grid of one CTA per SM, so CTAs that share an A
 // tile run at the same time.  Every wait is bounded (tc::mbar_wait); on a
@@ -55,8 +60,8 @@ struct GemmShape {
 
 template <int BN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
-              int K, Epi epi, int* err) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+              const __grid_constant__ CUtensorMap tmB, int M, int m_split, int N, int K, Epi epi, int* err) {
     using S = GemmShape<BN, Epi::kScratchWords>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -92,6 +97,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
+        if (m_split < (M + kBM - 1) / kBM) tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB);
     }
     tc_fence_before();
@@ -116,11 +122,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
                 const int m = t / n_tiles, n = t % n_tiles;
+                const bool second = m >= m_split;
+                const CUtensorMap* ta = second ? &tmA2 : &tmA;
+                const int arow = (second ? m - m_split : m) * kBM;
                 for (int kk = 0; kk < k_iters; ++kk) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) break;
                     const uint32_t sa = smem_u32(smem + (size_t)stage * S::STAGE);
                     mbar_arrive_expect_tx(full0 + 8 * stage, S::STAGE);
-                    tma_load_2d(sa, &tmA, kk * kBK, m * kBM, full0 + 8 * stage, pol_a);
+                    tma_load_2d(sa, ta, kk * kBK, arow, full0 + 8 * stage, pol_a);
                     tma_load_2d(sa + S::A_BYTES, &tmB, kk * kBK, n * BN, full0 + 8 * stage, pol_b);
                     ++issued;
                     if (++stage == S::STAGES) {

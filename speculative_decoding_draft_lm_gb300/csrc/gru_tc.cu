@@ -189,7 +189,8 @@ cudaError_t launch_gemm(domino_ctx* c, RunArgs& r, const CUtensorMap& tmA, const
     const int tiles = ((M + tc::kBM - 1) / tc::kBM) * ((r.B + BN - 1) / BN);
     const int grid = tiles < c->num_sms ? tiles : c->num_sms;
     ++r.launches;
-    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, tmA, tmB, M, r.B, K, epi, c->err);
+    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, tmA, tmA, tmB, M, INT_MAX, r.B, K, epi,
+                      c->err);
 }
 
 template <class Epi>

@@ -31,6 +31,7 @@ struct RunArgs {
     int B;
     int K;                     // effective pool size: 0 = full vocabulary
     int n_prop;                // proposals produced (1..15): p_1 + n_prop-1 corrected steps
+    void* s_out;               // non-null: compute s here ([B,15,F], input dtype); then s == s_out
     const int32_t* forced;     // nullable [B,15]
     domino_debug_bufs dbg;     // all-null when not debugging
     int32_t* out_tokens;       // [B,15]
@@ -56,8 +57,11 @@ cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint
 cudaError_t make_tmap_bf16_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                                    uint32_t box_rows);
 bool lmhead_tc_supported(const domino_ctx* c);
-// also writes p_1's argmax word and, when r.K > 0, the pool scores
+// also writes p_1's argmax word, when r.K > 0 the pool scores, and when
+// r.s_out is set the per-step term s of projector layer 1
 cudaError_t launch_lmhead_tc(domino_ctx* c, RunArgs& r);
+// s from the backbone hidden on the CUDA cores (paths without the tcgen05 LM-head)
+cudaError_t launch_backbone_s_simt(domino_ctx* c, RunArgs& r);
 
 // tcgen05 correction over the full vocabulary (correct_tc.cu)
 int correct_bn(int B);  // N tile of the batched tensor-core kernels

@@ -393,6 +393,34 @@ __global__ void k_finalize(const unsigned long long* __restrict__ keys, const in
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Per-step term of projector layer 1 from the backbone hidden (page "Add
+// correctness-first Domino support to DFlash V2": embed_proj over [backbone
+// hidden | GRU state]): s[b, j, f] = W_hid[f, :] . hidden[b, j+1, :], one warp
+// per output, stored in the input dtype.
+__device__ __forceinline__ void store_as(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_as(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_backbone_s(const T* __restrict__ hidden, const T* __restrict__ w,
+                                                    T* __restrict__ s, int B, int H, int F) {
+    const int lane = threadIdx.x & 31;
+    const long long total = (long long)B * kProposals * F;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wid < total;
+         wid += nwarps) {
+        const int f = (int)(wid % F);
+        const long long bj = wid / F;
+        const int b = (int)(bj / kProposals), j = (int)(bj % kProposals);
+        const T* x = hidden + ((size_t)b * kBlock + kRowOffset + j) * H;
+        const T* wr = w + (size_t)f * H;
+        float acc = 0.f;
+        for (int h = lane; h < H; h += 32) acc = fmaf(to_f32(x[h]), to_f32(wr[h]), acc);
+        acc = warp_sum(acc);
+        if (lane == 0) store_as(&s[((size_t)b * kProposals + j) * F + f], acc);
+    }
+}
+
 // ===========================================================================
 // host launchers
 #define DOMINO_LAUNCH_CHECK()                      \
@@ -417,6 +445,20 @@ cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r) {
     else
         k_lmhead_simt<__nv_bfloat16><<<grid, 256, 0, r.st>>>((const __nv_bfloat16*)r.hidden,
                                                              (const __nv_bfloat16*)c->lm_head, c->L, r.B, g.V, g.H);
+    DOMINO_LAUNCH_CHECK();
+    return cudaSuccess;
+}
+
+cudaError_t launch_backbone_s_simt(domino_ctx* c, RunArgs& r) {
+    const domino_config& g = c->cfg;
+    const int grid = grid_for(8, r.B * kProposals * g.F, c->num_sms * 8);
+    if (g.dtype == DOMINO_DTYPE_FP32)
+        k_backbone_s<float><<<grid, 256, 0, r.st>>>((const float*)r.hidden, (const float*)c->fc1_hid,
+                                                    (float*)r.s_out, r.B, g.H, g.F);
+    else
+        k_backbone_s<__nv_bfloat16><<<grid, 256, 0, r.st>>>((const __nv_bfloat16*)r.hidden,
+                                                            (const __nv_bfloat16*)c->fc1_hid,
+                                                            (__nv_bfloat16*)r.s_out, r.B, g.H, g.F);
     DOMINO_LAUNCH_CHECK();
     return cudaSuccess;
 }

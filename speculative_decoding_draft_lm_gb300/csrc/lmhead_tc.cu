@@ -11,6 +11,14 @@
 //
 // Orientation: vocabulary rows are the MMA's M (128 per tile, A = lm_head,
 // streamed once), the B*16 draft rows are N (B operand, L2-resident).
+//
+// When the per-step term s of projector layer 1 is computed in the library,
+// its weight W_hid [F, H] (the backbone-hidden half of that layer, page "Add
+// correctness-first Domino support to DFlash V2": embed_proj acts on
+// [backbone hidden | GRU state]) rides along as extra A rows after the
+// vocabulary, sharing the hidden-state operand:
+//   s[b, j, f] = sum_h hidden[b, j+1, h] * W_hid[f, h],  j = 0..14,
+// stored in the input dtype (bf16).
 #include "gemm_tc.cuh"
 #include "internal.h"
 
@@ -25,7 +33,8 @@ struct EpiLmHead {
     float* L;                  // [B,16,V]
     unsigned long long* keys;  // [B,16], slot 0 = p_1
     float* score;              // [B,V] or null
-    int V, B;
+    __nv_bfloat16* s_out;      // [B,15,F] or null: rows from s_row0 on are W_hid rows
+    int V, B, s_row0, F;
     __device__ __forceinline__ void begin(unsigned long long* sb, int t) const {
         for (int i = t; i < tc::kEpiScratch; i += tc::kEpiThreads) sb[i] = 0ull;
     }
@@ -40,6 +49,15 @@ struct EpiLmHead {
                                                unsigned long long* sb, const float*) const {
         const int b = col0 >> 4;  // 16 columns = the 16 block rows of request b
         if (b >= B) return;       // uniform across the warp
+        if (row >= s_row0) {      // uniform: s_row0 is a multiple of 128
+            const int f = row - s_row0;
+            if (f < F) {
+#pragma unroll
+                for (int i = kRowOffset; i < kRowOffset + kProposals; ++i)
+                    s_out[((size_t)b * kProposals + (i - kRowOffset)) * F + f] = __float2bfloat16_rn(v[i]);
+            }
+            return;
+        }
         const bool ok = row < V;
         if (ok) {
             float* dst = L + (size_t)b * kBlock * V + row;
@@ -86,12 +104,18 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, float* 
         attr_set[slot] = true;
     }
     const int N = r.B * kBlock;
-    const int tiles = ((c->cfg.V + tc::kBM - 1) / tc::kBM) * ((N + BN - 1) / BN);
+    const int v_tiles = (c->cfg.V + tc::kBM - 1) / tc::kBM;
+    const bool with_s = r.s_out != nullptr;
+    const int m_tiles = v_tiles + (with_s ? (c->cfg.F + tc::kBM - 1) / tc::kBM : 0);
+    const int tiles = m_tiles * ((N + BN - 1) / BN);
     const int grid = tiles < c->num_sms ? tiles : c->num_sms;
-    EpiLmHead epi{c->L, c->keys, score, c->cfg.V, r.B};
+    const int s_row0 = with_s ? v_tiles * tc::kBM : INT_MAX;
+    EpiLmHead epi{c->L, c->keys, score, (__nv_bfloat16*)r.s_out, c->cfg.V, r.B, s_row0, c->cfg.F};
     ++r.launches;
-    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_lm_head, tmB, c->cfg.V, N,
-                      c->cfg.H, epi, c->err);
+    const int M = with_s ? s_row0 + c->cfg.F : c->cfg.V;
+    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_lm_head,
+                      with_s ? c->tm_fc1h : c->tm_lm_head, tmB, M, with_s ? v_tiles : INT_MAX, N, c->cfg.H, epi,
+                      c->err);
 }
 
 }  // namespace

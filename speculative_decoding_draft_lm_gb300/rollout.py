@@ -38,7 +38,7 @@ EXPORTED = (
     "domino_rollout_debug_run", "domino_rollout_set_driver", "domino_rollout_status",
     "domino_rollout_last_launch_count", "domino_rollout_destroy", "domino_rollout_strerror",
     "domino_rollout_enable_timing", "domino_rollout_read_timing", "domino_candidate_pool_static",
-    "domino_rollout_set_proposals",
+    "domino_rollout_set_proposals", "domino_rollout_load_backbone_proj",
 )
 
 PHASES = ("lmhead", "argmax", "pool", "gru", "fc1", "correct", "steps", "other")
@@ -91,6 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.domino_rollout_read_timing.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
     lib.domino_candidate_pool_static.argtypes = [vp, i, i, i, vp, vp]
     lib.domino_rollout_set_proposals.argtypes = [vp, i]
+    lib.domino_rollout_load_backbone_proj.argtypes = [vp, vp]
     lib.domino_rollout_strerror.argtypes = [i]
     lib.domino_rollout_strerror.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -152,6 +153,11 @@ def domino_rollout_debug_run(ctx, hidden, s, verified_tok, B: int, K: int, force
 
 def domino_rollout_set_driver(ctx, driver: int) -> int:
     return _check(load_library().domino_rollout_set_driver(ctx, driver), "domino_rollout_set_driver")
+
+
+def domino_rollout_load_backbone_proj(ctx, w_hid) -> int:
+    return _check(load_library().domino_rollout_load_backbone_proj(ctx, _ptr(w_hid)),
+                  "domino_rollout_load_backbone_proj")
 
 
 def domino_rollout_set_proposals(ctx, n: int) -> int:
@@ -227,6 +233,13 @@ class DominoRollout:
         self._weights = dict(weights)  # keep them alive while borrowed
         domino_rollout_load_weights(self.ctx, weights["lm_head"], weights["emb"], weights["w_ih"],
                                     weights["w_hh"], weights["fc1"], weights["fc2"], weights["b"])
+
+    def load_backbone_proj(self, w_hid):
+        """Register W_hid [F, H]; then run(hidden, None, verified) derives s."""
+        if w_hid is not None:
+            self._check_tensor(w_hid, (self.dims["F"], self.dims["H"]), "w_hid")
+        self._w_hid = w_hid  # keep it alive while borrowed
+        domino_rollout_load_backbone_proj(self.ctx, w_hid)
 
     def set_driver(self, driver: int):
         domino_rollout_set_driver(self.ctx, driver)
