@@ -104,9 +104,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // setup above overlaps the previous kernel; everything below may read its output
+    // setup above overlaps the previous kernel.  The A operand is a weight
+    // matrix that no kernel writes, so the producer requests the first
+    // ring-full of A tiles before waiting for the previous kernel; everything
+    // else waits for it here.
     pdl_trigger();
-    pdl_wait();
+    if (warp != 0) pdl_wait();
 
     const int m_tiles = (M + kBM - 1) / kBM;
     const int n_tiles = (N + BN - 1) / BN;
@@ -118,18 +121,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_first();
             const uint64_t pol_b = policy_evict_last();
+            const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+            const int total = my_tiles * k_iters;
+            const int pre = total < S::STAGES ? total : S::STAGES;  // chunk i sits in stage i
+            auto a_row = [&](int t, const CUtensorMap*& ta) {
+                const int m = t / n_tiles;
+                const bool second = m >= m_split;
+                ta = second ? &tmA2 : &tmA;
+                return (second ? m - m_split : m) * kBM;
+            };
+            for (int i = 0; i < pre; ++i) {  // fresh ring: no slot to wait for
+                const int t = blockIdx.x + (i / k_iters) * gridDim.x, kk = i % k_iters;
+                const CUtensorMap* ta;
+                const int arow = a_row(t, ta);
+                mbar_arrive_expect_tx(full0 + 8 * i, S::STAGE);
+                tma_load_2d(smem_u32(smem + (size_t)i * S::STAGE), ta, kk * kBK, arow, full0 + 8 * i, pol_a);
+            }
+            pdl_wait();
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-                const int m = t / n_tiles, n = t % n_tiles;
-                const bool second = m >= m_split;
-                const CUtensorMap* ta = second ? &tmA2 : &tmA;
-                const int arow = (second ? m - m_split : m) * kBM;
-                for (int kk = 0; kk < k_iters; ++kk) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) break;
+            int i = 0;
+            // the pre-issued stages always get their B half (so that every copy
+            // in flight belongs to a stage the abort drain below can wait for)
+            for (int t = blockIdx.x; t < tiles && (i < pre || !*abort_flag); t += gridDim.x) {
+                const int n = t % n_tiles;
+                const CUtensorMap* ta;
+                const int arow = a_row(t, ta);
+                for (int kk = 0; kk < k_iters; ++kk, ++i) {
                     const uint32_t sa = smem_u32(smem + (size_t)stage * S::STAGE);
-                    mbar_arrive_expect_tx(full0 + 8 * stage, S::STAGE);
-                    tma_load_2d(sa, ta, kk * kBK, arow, full0 + 8 * stage, pol_a);
+                    if (i >= pre) {
+                        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) break;
+                        mbar_arrive_expect_tx(full0 + 8 * stage, S::STAGE);
+                        tma_load_2d(sa, ta, kk * kBK, arow, full0 + 8 * stage, pol_a);
+                    }
                     tma_load_2d(sa + S::A_BYTES, &tmB, kk * kBK, n * BN, full0 + 8 * stage, pol_b);
                     ++issued;
                     if (++stage == S::STAGES) {
