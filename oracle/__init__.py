@@ -5,6 +5,6 @@ import this package; the CUDA library never does.
 """
 from .domino_oracle import (  # noqa: F401
     BLOCK, N_PROPOSALS, N_CORRECTED, ROW_OFFSET, OracleWeights, argmax_lowest, backbone_s,
-    candidate_pool, gru_cell, lm_head, rollout, run, silu, sigmoid, top2_margin,
+    candidate_pool, candidate_pool_compact, gru_cell, lm_head, rollout, run, silu, sigmoid, top2_margin,
     widen,
 )

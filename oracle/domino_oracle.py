@@ -125,6 +125,33 @@ def candidate_pool(L_rows: np.ndarray, K: int) -> np.ndarray:
     return np.sort(order[:K])
 
 
+def candidate_pool_compact(L_rows: np.ndarray, K: int, P: int) -> np.ndarray:
+    """The same pool built the way the tensor-parallel stage C builds it.
+
+    Page "feat: support tensor-parallel Domino rollout", section
+    "Implementation", stage C: each of P ranks owns a contiguous vocabulary
+    shard, takes its local top-K, and the P*K candidates are merged into the
+    global top-K.  Shards are [p*S, min(V, (p+1)*S)) with S = ceil(V/P); both
+    selections order by (score desc, id asc).  Returned in ascending id order.
+    """
+    V = L_rows.shape[1]
+    if K <= 0 or K >= V:
+        return np.arange(V, dtype=np.int64)
+    score = L_rows.max(axis=0)
+    S = -(-V // P)
+    cand = []
+    for p in range(P):
+        lo, hi = p * S, min(V, (p + 1) * S)
+        if lo >= hi:
+            continue
+        ids = np.arange(lo, hi)
+        order = np.lexsort((ids, -score[lo:hi]))
+        cand.append(ids[order[:K]])
+    cand = np.concatenate(cand)
+    order = np.lexsort((cand, -score[cand]))
+    return np.sort(cand[order[:K]])
+
+
 class OracleWeights:
     """Weights widened once to float64 (the analogue of load_weights)."""
 

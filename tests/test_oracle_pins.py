@@ -314,3 +314,27 @@ def test_backbone_s_matches_explicit_s_and_brute_force():
     np.testing.assert_array_equal(a["z"], c["z"])
     with pytest.raises(ValueError):
         oracle.rollout(oracle.OracleWeights(w), r["hidden"], None, r["verified"], 0)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 7, 8])
+def test_compact_pool_merge_equals_full_selection(P):
+    """Stage C (shard-local top-K, then a global merge) selects exactly the
+    stage B pool, ties included (the pages report B and C proposals equal)."""
+    rng = np.random.default_rng(P)
+    for trial in range(20):
+        V = int(rng.integers(50, 400))
+        K = int(rng.integers(1, V))
+        rows = rng.standard_normal((15, V))
+        if trial % 2:  # heavy ties: few distinct values
+            rows = np.round(rows * 2) / 2
+        want = oracle.candidate_pool(rows, K)
+        got = oracle.candidate_pool_compact(rows, K, P)
+        assert (got == want).all(), (P, V, K)
+
+
+def test_compact_pool_brute_force_tiny():
+    rows = np.array([[3.0, 1.0, 3.0, 2.0, 3.0, 0.0, 1.0]] * 15)
+    # shards of 4 and 3 ids; top-3 by (score desc, id asc): ids 0, 2, 4
+    assert oracle.candidate_pool_compact(rows, 3, 2).tolist() == [0, 2, 4]
+    assert oracle.candidate_pool_compact(rows, 2, 2).tolist() == [0, 2]
+    assert oracle.candidate_pool_compact(rows, 4, 3).tolist() == [0, 2, 3, 4]
