@@ -503,14 +503,18 @@ def main():
     # K0 with s derived in the library from the backbone hidden rows
     if sweep:
         table = {}
-        runs = ([(n, 15, False) for n in sweep] + [(n, 7, False) for n in sweep if inputs.WORKLOADS[n].B <= 8] +
-                [(n, 15, True) for n in sweep if inputs.WORKLOADS[n].K == 0])
+        # (workload, proposals, s in the library, vocabulary shards of the pool)
+        runs = ([(n, 15, False, 1) for n in sweep] +
+                [(n, 7, False, 1) for n in sweep if inputs.WORKLOADS[n].B <= 8] +
+                [(n, 15, True, 1) for n in sweep if inputs.WORKLOADS[n].K == 0] +
+                [(n, 15, False, 2) for n in sweep if inputs.WORKLOADS[n].K > 0])
         if any(r_[2] for r_ in runs):
             w_hid = to_device(inputs.make_fc1_hidden(sh, seed=5))
             eng.load_backbone_proj(w_hid)
-        for name, n_prop, own_s in runs:
+        for name, n_prop, own_s, parts in runs:
             w2 = inputs.WORKLOADS[name]
             eng.set_proposals(n_prop)
+            eng.set_vocab_partitions(parts)
             rq = inputs.make_requests(sh, list(w2.request_seeds))
             h2, s2, v2 = to_device(rq["hidden"]), to_device(rq["s"]), torch.from_numpy(rq["verified"]).cuda()
             if own_s:
@@ -549,15 +553,18 @@ def main():
             ms = sum(tt) / len(tt)
             ab2 = alg_bytes(sh, w2.B, w2.K, n_prop, own_s)
             lm_avg = lm_ms / max(1, lm_n)
-            label = name + ("" if n_prop == 15 else f"_n{n_prop}") + ("_s_in_library" if own_s else "")
+            label = (name + ("" if n_prop == 15 else f"_n{n_prop}") + ("_s_in_library" if own_s else "") +
+                     ("" if parts == 1 else f"_compact_pool_p{parts}"))
             table[label] = {
                 "us_per_block": ms * 1e3, "proposals": n_prop, "s": "in library" if own_s else "input",
+                "vocab_partitions": parts,
                 "proposals_per_s": float(n_prop) * w2.B / (ms * 1e-3),
                 "hbm_frac_block": ab2["block"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "lmhead_us": lm_avg * 1e3,
                 "lmhead_tensor_frac": ab2["lmhead_flop"] / (lm_avg * 1e-3) / 1e12 / peaks["bf16_tflops"],
                 "phase_us_timed_pass": {k_: m_ * 1e3 / n_sweep for k_, m_ in ph_ms.items()}}
         eng.set_proposals(15)
+        eng.set_vocab_partitions(1)
         torch.cuda.synchronize()
         if eng.status() != 0:
             raise RuntimeError("device error during the sweep")

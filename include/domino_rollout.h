@@ -182,6 +182,19 @@ DOMINO_API int domino_rollout_read_timing(domino_ctx* ctx, float* ms, int* launc
  * this context.  Errors: INVALID_ARG (null ctx or n outside 1..15). */
 DOMINO_API int domino_rollout_set_proposals(domino_ctx* ctx, int n);
 
+/* Candidate-pool construction of the tensor-parallel stage C, on one GPU
+ * (page "feat: support tensor-parallel Domino rollout", section
+ * "Implementation": each rank takes a local top-K of its vocabulary shard and
+ * the candidates are merged to the global top-K).  P > 1 splits the
+ * vocabulary into P contiguous shards of ceil(V/P) ids: one cluster
+ * radix-select per (request, shard), then one per request over the P*K
+ * candidates.  The pool is the same as with P = 1 (the direct selection),
+ * ties included; only the way it is built changes.  P = 1 (default) .. 8.
+ * Pool modes with K > 0 only; ignored when the selection does not fit.
+ * Errors: INVALID_ARG. */
+#define DOMINO_MAX_VOCAB_PARTITIONS 8
+DOMINO_API int domino_rollout_set_vocab_partitions(domino_ctx* ctx, int P);
+
 /* Synchronise `cuda_stream`, then return and clear the device error word
  * (DOMINO_OK, DOMINO_ERR_BAD_TOKEN or DOMINO_ERR_TIMEOUT), or DOMINO_ERR_CUDA
  * if the stream reported an error. */

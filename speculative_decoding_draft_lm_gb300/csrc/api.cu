@@ -115,7 +115,14 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
             if (r.s_out) STEP(DOMINO_PHASE_LMHEAD, launch_backbone_s_simt(c, r));
             STEP(DOMINO_PHASE_ARGMAX, launch_first_argmax(c, r));
         }
-        if (r.K > 0) STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, tc_path));
+        if (r.K > 0) {
+            if (c->partitions > 1 && pool_compact_supported(c, c->partitions, r.K)) {
+                if (!tc_path) STEP(DOMINO_PHASE_POOL, launch_score(c, r));
+                STEP(DOMINO_PHASE_POOL, launch_pool_compact(c, r, c->partitions));
+            } else {
+                STEP(DOMINO_PHASE_POOL, launch_pool_select(c, r, tc_path));
+            }
+        }
     }
     if (use_persist) {
         STEP(DOMINO_PHASE_STEPS, launch_persist(c, r));
@@ -218,6 +225,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oX = take(gru_tc ? (size_t)2 * c->a_rows * ldx * 2 : 0);
     const bool pmask = g.max_K > 0 && g.dtype == DOMINO_DTYPE_BF16;
     size_t oM = take(pmask ? (size_t)g.max_B * pool_mask_words(g.V) * 4 : 0);
+    size_t oC = take(g.max_K > 0 ? (size_t)g.max_B * DOMINO_MAX_VOCAB_PARTITIONS * g.max_K * 4 : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -239,6 +247,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->wp = gru_tc ? (__nv_bfloat16*)(base + oWp) : nullptr;
     c->xh16 = gru_tc ? (__nv_bfloat16*)(base + oX) : nullptr;
     c->pmask = pmask ? (uint32_t*)(base + oM) : nullptr;
+    c->cand = g.max_K > 0 ? (int32_t*)(base + oC) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -248,6 +257,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     }
     c->driver = DOMINO_DRIVER_AUTO;
     c->n_proposals = kProposals;
+    c->partitions = 1;
     *out = c;
     return DOMINO_OK;
 }
@@ -346,6 +356,12 @@ int domino_rollout_read_timing(domino_ctx* c, float* ms, int* launches) {
         }
     }
     c->n_pending = 0;
+    return DOMINO_OK;
+}
+
+int domino_rollout_set_vocab_partitions(domino_ctx* c, int P) {
+    if (!c || P < 1 || P > DOMINO_MAX_VOCAB_PARTITIONS) return DOMINO_ERR_INVALID_ARG;
+    c->partitions = P;
     return DOMINO_OK;
 }
 

@@ -175,6 +175,7 @@ struct domino_ctx {
     int num_sms;
     int driver;
     int n_proposals;  // early stop: proposals per block (1..15)
+    int partitions;   // vocabulary shards of the compact pool construction (1 = direct)
     int last_launches;
     bool loaded;
     // borrowed weights
@@ -185,6 +186,7 @@ struct domino_ctx {
     float* score;             // [max_B,V]
     int32_t* pool;            // [max_B,max_K]
     void* s_ws;               // [max_B,15,F] input dtype: s computed from the backbone hidden
+    int32_t* cand;            // [max_B, DOMINO_MAX_VOCAB_PARTITIONS*max_K] stage-C candidates, or null
     uint32_t* pmask;          // [max_B, ceil(V/32)] pool membership bits (bf16, max_K > 0), or null
     float* h;                 // [2][max_B,G] ping-pong
     float* a;                 // [max_B,F]

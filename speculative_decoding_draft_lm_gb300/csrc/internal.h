@@ -44,6 +44,7 @@ cudaError_t launch_reset(domino_ctx* c, RunArgs& r);
 cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r);
 cudaError_t launch_first_argmax(domino_ctx* c, RunArgs& r);
 cudaError_t launch_pool_select(domino_ctx* c, RunArgs& r, bool score_ready);
+cudaError_t launch_score(domino_ctx* c, RunArgs& r);  // pool scores from the base logits
 // GRU update u (0..14): u = 0 consumes the verified token with h = 0,
 // u >= 1 consumes proposal u-1 (or forced[:,u-1]).
 cudaError_t launch_gru(domino_ctx* c, RunArgs& r, int u);
@@ -77,6 +78,9 @@ bool pool_cluster_supported(const domino_ctx* c);
 cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r);
 cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, int V, int K, cudaStream_t st);
 bool pool_cluster_fits(int V);
+// stage C of the tensor-parallel rollout on one GPU: P shard-local top-K, then the merge
+bool pool_compact_supported(const domino_ctx* c, int P, int K);
+cudaError_t launch_pool_compact(domino_ctx* c, RunArgs& r, int P);
 
 // batched GRU / projector layer 1 for B >= 2 (kernels_batch.cu)
 bool batch_kernels_supported(const domino_ctx* c);

@@ -470,11 +470,17 @@ cudaError_t launch_first_argmax(domino_ctx* c, RunArgs& r) {
     return cudaSuccess;
 }
 
+cudaError_t launch_score(domino_ctx* c, RunArgs& r) {
+    int grid = grid_for(256, r.B * c->cfg.V, c->num_sms * 8);
+    k_score<<<grid, 256, 0, r.st>>>(c->L, c->score, r.B, c->cfg.V);
+    DOMINO_LAUNCH_CHECK();
+    return cudaSuccess;
+}
+
 cudaError_t launch_pool_select(domino_ctx* c, RunArgs& r, bool score_ready) {
     if (!score_ready) {
-        int grid = grid_for(256, r.B * c->cfg.V, c->num_sms * 8);
-        k_score<<<grid, 256, 0, r.st>>>(c->L, c->score, r.B, c->cfg.V);
-        DOMINO_LAUNCH_CHECK();
+        cudaError_t e = launch_score(c, r);
+        if (e != cudaSuccess) return e;
     }
     if (pool_cluster_supported(c)) return launch_pool_cluster(c, r);
     k_pool_select<<<r.B, 1024, 0, r.st>>>(c->score, c->pool, c->cfg.V, r.K);

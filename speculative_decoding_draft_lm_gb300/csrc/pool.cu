@@ -14,6 +14,17 @@
 // key > T and the lowest-id `need` ids with key == T are then written, each
 // CTA at the offset given by the counts of the CTAs before it, so the pool
 // comes out in ascending order without a sort.
+//
+// The same kernel runs the two passes of the tensor-parallel compact pool
+// (page "feat: support tensor-parallel Domino rollout", section
+// "Implementation", stage C), emulated on one GPU with P vocabulary shards:
+//   pass 1, one row per (request, shard): the shard-local top-K of the
+//           shard's scores [p*S, min(V, (p+1)*S)), S = ceil(V/P); a shard
+//           shorter than K gives all its ids and pads its K slots with -1;
+//   pass 2, one row per request: the top-K of the P*K candidates, whose
+//           scores are gathered through their ids (padding ranks lowest).
+// Both order by (score desc, id asc), and the candidates of a request are in
+// ascending id order, so pass 2 returns exactly the direct pool.
 #include <cooperative_groups.h>
 
 #include "internal.h"
@@ -64,22 +75,44 @@ __device__ __forceinline__ unsigned block_scan_excl(unsigned x, unsigned* warp_t
     return r;
 }
 
-__global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* __restrict__ score,
-                                                                 int32_t* __restrict__ pool, int V, int K,
-                                                                 int chunk) {
+// Row y of the grid: request b = y / shards, shard p = y % shards.
+// cand == null: select among score[b*stride + p*shard_len + i], i < min(shard_len, V - p*shard_len),
+//               writing vocabulary ids to pool[b*out_stride + p*K + j];
+// cand != null: (shards == 1) select among the V candidates cand[b*V + i] (id -1 = none) by
+//               score[b*stride + id], writing the candidate ids to pool[b*out_stride + j].
+__global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* __restrict__ score, long long stride,
+                                                                 const int32_t* __restrict__ cand, int shards,
+                                                                 int shard_len, int32_t* __restrict__ pool,
+                                                                 int out_stride, int V, int K, int chunk) {
     extern __shared__ __align__(16) uint8_t smem[];
     PoolShared& S = *reinterpret_cast<PoolShared*>(smem);
     unsigned* keys = reinterpret_cast<unsigned*>(smem + sizeof(PoolShared));
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
-    const int b = blockIdx.y;
+    const int b = blockIdx.y / shards, shard = blockIdx.y % shards;
     const int lane = threadIdx.x & 31;
-    const int v0 = min(V, rank * chunk), v1 = min(V, v0 + chunk), n = v1 - v0;
+    const int lo = shard * shard_len;
+    const int n_row = min(shard_len, V - lo);
+    const int Kr = min(K, n_row);
+    const int v0 = min(n_row, rank * chunk), v1 = min(n_row, v0 + chunk), n = v1 - v0;
 
-    const float* sc = score + (size_t)b * V + v0;
-    for (int i = threadIdx.x; i < n; i += kPoolThreads) keys[i] = ord_f32(sc[i]);
+    const float* srow = score + (size_t)b * stride;
+    const int32_t* crow = cand ? cand + (size_t)b * V + v0 : nullptr;
+    if (cand) {
+        // key 0 is below every finite score's key: padding never outranks a real id
+        for (int i = threadIdx.x; i < n; i += kPoolThreads) {
+            const int id = crow[i];
+            keys[i] = id >= 0 ? ord_f32(srow[id]) : 0u;
+        }
+    } else {
+        for (int i = threadIdx.x; i < n; i += kPoolThreads) keys[i] = ord_f32(srow[lo + v0 + i]);
+    }
+    int32_t* out = pool + (size_t)b * out_stride + (size_t)shard * K;
+    if (rank == 0)
+        for (int j = (Kr > 0 ? Kr : 0) + threadIdx.x; j < K; j += kPoolThreads) out[j] = -1;
+    if (Kr <= 0) return;  // an empty shard: the whole cluster (one row) leaves together
 
-    unsigned prefix = 0, pmask = 0, remaining = (unsigned)K;
+    unsigned prefix = 0, pmask = 0, remaining = (unsigned)Kr;
     const int shifts[3] = {21, 10, 0};
     const int widths[3] = {11, 11, 10};
 #pragma unroll 1
@@ -197,7 +230,6 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
     const unsigned eq_take = eq_before >= need ? 0u : min(eq, need - eq_before);
     // ids written before this thread: all greater ones, and the equal ones taken so far
     unsigned pos = gt_before_r + gt_before_t + min(need, eq_before);
-    int32_t* out = pool + (size_t)b * K;
     unsigned eq_used = 0;
     for (int i = i0; i < i1; ++i) {
         const unsigned k = keys[i];
@@ -206,21 +238,23 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
             take = true;
             ++eq_used;
         }
-        if (take && pos < (unsigned)K) out[pos++] = v0 + i;
+        if (take && pos < (unsigned)Kr) out[pos++] = cand ? crow[i] : lo + v0 + i;
     }
     cluster.sync();  // no CTA leaves while others may still read its shared memory
 }
 
 }  // namespace
 
-// Pool selection from caller-given scores: the same kernel, pointers passed in.
-cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, int V, int K, cudaStream_t st) {
-    const int chunk = (V + kRanks - 1) / kRanks;
+namespace {
+
+cudaError_t launch_rows(const float* score, long long stride, const int32_t* cand, int shards, int shard_len,
+                        int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st) {
+    const int chunk = (shard_len + kRanks - 1) / kRanks;
     const size_t smem = sizeof(PoolShared) + (size_t)chunk * 4;
     cudaError_t e = cudaFuncSetAttribute(k_pool_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kRanks, B);
+    cfg.gridDim = dim3(kRanks, B * shards);
     cfg.blockDim = dim3(kPoolThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -231,39 +265,43 @@ cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_pool_cluster, score, pool, V, K, chunk);
+    return cudaLaunchKernelEx(&cfg, k_pool_cluster, score, stride, cand, shards, shard_len, pool, out_stride, V, K,
+                              chunk);
 }
 
-bool pool_cluster_fits(int V) {
-    const int chunk = (V + kRanks - 1) / kRanks;
-    return sizeof(PoolShared) + (size_t)chunk * 4 <= 220 * 1024;
+bool fits(int row_len) { return sizeof(PoolShared) + (size_t)((row_len + kRanks - 1) / kRanks) * 4 <= 220 * 1024; }
+
+}  // namespace
+
+// Pool selection from caller-given scores: the same kernel, pointers passed in.
+cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, int V, int K, cudaStream_t st) {
+    return launch_rows(score, V, nullptr, 1, V, pool, K, B, V, K, st);
 }
 
-bool pool_cluster_supported(const domino_ctx* c) {
-    const int chunk = (c->cfg.V + kRanks - 1) / kRanks;
-    return sizeof(PoolShared) + (size_t)chunk * 4 <= 220 * 1024;
-}
+bool pool_cluster_fits(int V) { return fits(V); }
+
+bool pool_cluster_supported(const domino_ctx* c) { return fits(c->cfg.V); }
 
 cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r) {
-    const int chunk = (c->cfg.V + kRanks - 1) / kRanks;
-    const size_t smem = sizeof(PoolShared) + (size_t)chunk * 4;
-    cudaError_t e = cudaFuncSetAttribute(k_pool_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kRanks, r.B);
-    cfg.blockDim = dim3(kPoolThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = r.st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kRanks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_pool_cluster, (const float*)c->score, c->pool, c->cfg.V, r.K, chunk);
     ++r.launches;
-    return e;
+    return launch_rows(c->score, c->cfg.V, nullptr, 1, c->cfg.V, c->pool, r.K, r.B, c->cfg.V, r.K, r.st);
+}
+
+bool pool_compact_supported(const domino_ctx* c, int P, int K) {
+    return P >= 2 && P <= DOMINO_MAX_VOCAB_PARTITIONS && c->cand != nullptr && K <= c->cfg.max_K &&
+           fits((c->cfg.V + P - 1) / P) && fits(P * K);
+}
+
+cudaError_t launch_pool_compact(domino_ctx* c, RunArgs& r, int P) {
+    const int V = c->cfg.V, K = r.K;
+    const int S = (V + P - 1) / P;
+    // pass 1: shard-local top-K of every (request, shard) into cand [B, P*K]
+    ++r.launches;
+    cudaError_t e = launch_rows(c->score, V, nullptr, P, S, c->cand, P * K, r.B, V, K, r.st);
+    if (e != cudaSuccess) return e;
+    // pass 2: the global top-K among each request's P*K candidates
+    ++r.launches;
+    return launch_rows(c->score, V, c->cand, 1, P * K, c->pool, K, r.B, P * K, K, r.st);
 }
 
 }  // namespace domino

@@ -38,7 +38,7 @@ EXPORTED = (
     "domino_rollout_debug_run", "domino_rollout_set_driver", "domino_rollout_status",
     "domino_rollout_last_launch_count", "domino_rollout_destroy", "domino_rollout_strerror",
     "domino_rollout_enable_timing", "domino_rollout_read_timing", "domino_candidate_pool_static",
-    "domino_rollout_set_proposals", "domino_rollout_load_backbone_proj",
+    "domino_rollout_set_proposals", "domino_rollout_load_backbone_proj", "domino_rollout_set_vocab_partitions",
 )
 
 PHASES = ("lmhead", "argmax", "pool", "gru", "fc1", "correct", "steps", "other")
@@ -92,6 +92,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.domino_candidate_pool_static.argtypes = [vp, i, i, i, vp, vp]
     lib.domino_rollout_set_proposals.argtypes = [vp, i]
     lib.domino_rollout_load_backbone_proj.argtypes = [vp, vp]
+    lib.domino_rollout_set_vocab_partitions.argtypes = [vp, i]
     lib.domino_rollout_strerror.argtypes = [i]
     lib.domino_rollout_strerror.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -158,6 +159,10 @@ def domino_rollout_set_driver(ctx, driver: int) -> int:
 def domino_rollout_load_backbone_proj(ctx, w_hid) -> int:
     return _check(load_library().domino_rollout_load_backbone_proj(ctx, _ptr(w_hid)),
                   "domino_rollout_load_backbone_proj")
+
+
+def domino_rollout_set_vocab_partitions(ctx, P: int) -> int:
+    return _check(load_library().domino_rollout_set_vocab_partitions(ctx, P), "domino_rollout_set_vocab_partitions")
 
 
 def domino_rollout_set_proposals(ctx, n: int) -> int:
@@ -246,6 +251,9 @@ class DominoRollout:
 
     def set_proposals(self, n: int):
         domino_rollout_set_proposals(self.ctx, n)
+
+    def set_vocab_partitions(self, P: int):
+        domino_rollout_set_vocab_partitions(self.ctx, P)
 
     def run(self, hidden, s, verified, K=0, out=None, stream=None):
         import torch
