@@ -79,7 +79,9 @@ def alg_bytes(sh: inputs.Shape, B: int, K: int, n_prop: int = 15, s_in_library: 
         corr = V * F * e + V * e + B * V * 4 + B * F * 4
     else:
         corr = B * K * (F * e + e + 4 + 4) + B * F * 4
-    gru = 3 * G * (E + G) * e + B * (E * e + G * 4 * 2)
+    # GRU: W_hh, plus per request one row of the token table (3G fp32: the
+    # input side W_ih emb[t], built at load time) and the state in and out
+    gru = 3 * G * G * e + B * (3 * G * 4 + G * 4 * 2)
     fc1 = F * G * e + B * (G * 4 + F * e + F * 4 * 2)
     pool = 0 if full else B * 15 * V * 4 + B * V * 4 * 5 + B * K * 4
     # persistent driver: the GRU seed and the corrected steps in one launch

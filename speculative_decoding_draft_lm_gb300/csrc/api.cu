@@ -220,9 +220,9 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oErr = take(sizeof(int));
     size_t oSync = take(1024);
     const bool gru_tc = gru_tc_shape_ok(g);
-    const size_t ldx = (size_t)g.E + g.G;
-    size_t oWp = take(gru_tc ? (size_t)4 * gru_padded_units(g.G) * ldx * 2 : 0);
-    size_t oX = take(gru_tc ? (size_t)2 * c->a_rows * ldx * 2 : 0);
+    size_t oWp = take(gru_tc ? (size_t)4 * gru_padded_units(g.G) * g.G * 2 : 0);
+    size_t oX = take(gru_tc ? (size_t)2 * c->a_rows * g.G * 2 : 0);
+    size_t oT = take((size_t)g.V * 3 * g.G * sizeof(float));
     const bool pmask = g.max_K > 0 && g.dtype == DOMINO_DTYPE_BF16;
     size_t oM = take(pmask ? (size_t)g.max_B * pool_mask_words(g.V) * 4 : 0);
     size_t oC = take(g.max_K > 0 ? (size_t)g.max_B * DOMINO_MAX_VOCAB_PARTITIONS * g.max_K * 4 : 0);
@@ -245,7 +245,8 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->err = (int*)(base + oErr);
     c->sync = (unsigned int*)(base + oSync);
     c->wp = gru_tc ? (__nv_bfloat16*)(base + oWp) : nullptr;
-    c->xh16 = gru_tc ? (__nv_bfloat16*)(base + oX) : nullptr;
+    c->h16 = gru_tc ? (__nv_bfloat16*)(base + oX) : nullptr;
+    c->gi_table = (float*)(base + oT);
     c->pmask = pmask ? (uint32_t*)(base + oM) : nullptr;
     c->cand = g.max_K > 0 ? (int32_t*)(base + oC) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
@@ -284,12 +285,22 @@ int domino_rollout_load_weights(domino_ctx* c, const void* lm_head, const void* 
             c->loaded = false;
             return DOMINO_ERR_CUDA;
         }
-        // the batched GRU contracts a packed copy of w_ih / w_hh (built here, once)
-        if (c->wp && (pack_gru_weights(c, 0) != cudaSuccess || cudaStreamSynchronize(0) != cudaSuccess)) {
+        c->has_tma = true;
+        // the batched GRU contracts a packed copy of w_hh (built here, once)
+        if (c->wp && pack_gru_weights(c, 0) != cudaSuccess) {
             c->loaded = false;
             return DOMINO_ERR_CUDA;
         }
-        c->has_tma = true;
+    }
+    {
+        // input-side GRU pre-activations of every token (W_ih emb[v]), once
+        DeviceGuard guard(c->device);
+        int err_word = 0;
+        if (build_gi_table(c, 0) != cudaSuccess || cudaStreamSynchronize(0) != cudaSuccess ||
+            cudaMemcpy(&err_word, c->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess || err_word != 0) {
+            c->loaded = false;
+            return DOMINO_ERR_CUDA;
+        }
     }
     c->loaded = true;
     return DOMINO_OK;

@@ -196,8 +196,9 @@ struct domino_ctx {
     int* bad;                 // [max_B] request saw an invalid token
     int* err;                 // device error word
     unsigned int* sync;       // grid-barrier words for the persistent driver
-    __nv_bfloat16* wp;        // [4*Gp, E+G] packed GRU weights (bf16 batches), or null
-    __nv_bfloat16* xh16;      // [2][a_rows, E+G] GRU operand rows [emb | bf16 h]
+    float* gi_table;          // [V, 3G] input-side GRU pre-activations of every token (built at load)
+    __nv_bfloat16* wp;        // [4*Gp, G] packed hidden-side GRU weights (bf16 batches), or null
+    __nv_bfloat16* h16;       // [2][a_rows, G] bf16 copies of the GRU state (tensor-core operands)
     void* ws_base;            // single workspace allocation
     size_t ws_bytes;
     // TMA descriptors (bf16 path)

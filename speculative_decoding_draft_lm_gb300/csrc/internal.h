@@ -84,15 +84,18 @@ cudaError_t launch_pool_compact(domino_ctx* c, RunArgs& r, int P);
 
 // batched GRU / projector layer 1 for B >= 2 (kernels_batch.cu)
 bool batch_kernels_supported(const domino_ctx* c);
-cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u);
+// h16_out (nullable [B,G]): also store the new state as bf16 (tensor-core operand)
+cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u, __nv_bfloat16* h16_out = nullptr);
 cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k);
 bool pool_batch_supported(const domino_ctx* c);
 cudaError_t launch_correct_pool_batch(domino_ctx* c, RunArgs& r, int k);
 
-// tcgen05 GRU update and projector layer 1 for B >= 2 (gru_tc.cu)
+// input-side GRU pre-activations T[v, 3G] of every token (gi_table.cu)
+cudaError_t build_gi_table(domino_ctx* c, cudaStream_t st);
+
+// tcgen05 GRU update and projector layer 1 for batches (gru_tc.cu)
 struct GruMaps {
-    CUtensorMap x[2];  // operand rows [emb | bf16 h] of X[0], X[1]
-    CUtensorMap h[2];  // the state columns of X[0], X[1]
+    CUtensorMap h[2];  // the bf16 state copies H16[0], H16[1] (B operand of both contractions)
     CUtensorMap fc1;
 };
 int gru_padded_units(int G);

@@ -8,10 +8,11 @@
 // Projector layer 1 (page "[Spec] Add Domino projector support to DFlash
 // speculative decoding (V2)", section "Implementation"): a = SiLU(fc1 h + s).
 //
-// Layout: a CTA owns JT consecutive state elements j (3 gate rows of W_ih
-// and of W_hh each), staged once in shared memory; each warp takes requests
-// in turn, holds the request's embedding row and state in registers (lane l
-// owns elements (l + 32c)*8 .. +7) and forms all 6*JT dot products from them.
+// Layout: a CTA owns JT consecutive state elements j (3 gate rows of W_hh),
+// staged once in shared memory; each warp takes requests in turn, holds the
+// request's state in registers (lane l owns elements (l + 32c)*8 .. +7) and
+// forms the 3*JT hidden-side dot products from them.  The input side W_ih x
+// is row x of the table of every token's input pre-activations.
 #include "internal.h"
 
 namespace domino {
@@ -109,18 +110,16 @@ __device__ __forceinline__ void stage_rows(T* dst, const T* src_base, int row0, 
 
 template <typename T, int NCH>
 __global__ void __launch_bounds__(kBatchThreads) k_gru_batch(
-    const T* __restrict__ emb, const T* __restrict__ w_ih, const T* __restrict__ w_hh, const float* __restrict__ h_in,
-    float* __restrict__ h_out, const int32_t* __restrict__ verified, const int32_t* __restrict__ forced,
-    const unsigned long long* __restrict__ keys, int* __restrict__ bad, int* __restrict__ err,
-    float* __restrict__ dbg_h, int u, int B, int V, int E, int G) {
+    const float* __restrict__ gi_table, const T* __restrict__ w_hh, const float* __restrict__ h_in,
+    float* __restrict__ h_out, __nv_bfloat16* __restrict__ h16_out, const int32_t* __restrict__ verified,
+    const int32_t* __restrict__ forced, const unsigned long long* __restrict__ keys, int* __restrict__ bad,
+    int* __restrict__ err, float* __restrict__ dbg_h, int u, int B, int V, int G) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int j0 = blockIdx.x * kJT;
     const int jn = min(kJT, G - j0);
-    T* s_ih = reinterpret_cast<T*>(smem);                      // [3*jn][E]
-    T* s_hh = s_ih + (size_t)3 * kJT * E;                      // [3*jn][G]
+    T* s_hh = reinterpret_cast<T*>(smem);  // [3*jn][G]
     pdl_trigger();
     // weights do not depend on the previous kernel: stage them before waiting
-    stage_rows(s_ih, w_ih, j0, jn, G, E);
     if (u > 0) stage_rows(s_hh, w_hh, j0, jn, G, G);
     cp_wait();
     __syncthreads();
@@ -138,36 +137,32 @@ __global__ void __launch_bounds__(kBatchThreads) k_gru_batch(
             }
             t = 0;
         }
-        VecRegs<T, NCH> x;
-        x.load_t(emb + (size_t)t * E, E, lane);
-        VecRegs<T, NCH> hv;
-        if (u > 0) hv.load_f(h_in + (size_t)b * G, G, lane);
-        float gi[3 * kJT], gh[3 * kJT];
+        float gh[3 * kJT];
 #pragma unroll
-        for (int i = 0; i < 3 * kJT; ++i) {
-            gi[i] = 0.f;
-            gh[i] = 0.f;
-            if (i / kJT < 3 && (i % kJT) < jn) {
-                const int g = i / kJT, jj = i % kJT;
-                gi[i] = warp_sum(part_dot(s_ih + (size_t)(g * jn + jj) * E, x, E, lane));
-                if (u > 0) gh[i] = warp_sum(part_dot(s_hh + (size_t)(g * jn + jj) * G, hv, G, lane));
-            }
+        for (int i = 0; i < 3 * kJT; ++i) gh[i] = 0.f;
+        if (u > 0) {
+            VecRegs<T, NCH> hv;
+            hv.load_f(h_in + (size_t)b * G, G, lane);
+#pragma unroll
+            for (int i = 0; i < 3 * kJT; ++i)
+                if (i % kJT < jn) gh[i] = warp_sum(part_dot(s_hh + (size_t)((i / kJT) * jn + i % kJT) * G, hv, G, lane));
         }
         if (lane < jn) {
-            float ir = 0, iz = 0, in_ = 0, hr = 0, hz = 0, hn = 0;
+            float hr = 0, hz = 0, hn = 0;
 #pragma unroll
             for (int jj = 0; jj < kJT; ++jj)
                 if (jj == lane) {
-                    ir = gi[0 * kJT + jj]; iz = gi[1 * kJT + jj]; in_ = gi[2 * kJT + jj];
                     hr = gh[0 * kJT + jj]; hz = gh[1 * kJT + jj]; hn = gh[2 * kJT + jj];
                 }
             const int j = j0 + lane;
-            const float r = sigmoidf_(ir + hr);
-            const float zg = sigmoidf_(iz + hz);
-            const float n = tanhf(in_ + r * hn);
+            const float* gi = gi_table + (size_t)t * 3 * G;
+            const float r = sigmoidf_(gi[j] + hr);
+            const float zg = sigmoidf_(gi[G + j] + hz);
+            const float n = tanhf(gi[2 * G + j] + r * hn);
             const float hp = u > 0 ? h_in[(size_t)b * G + j] : 0.f;
             const float out = (1.f - zg) * n + zg * hp;
             h_out[(size_t)b * G + j] = out;
+            if (h16_out) h16_out[(size_t)b * G + j] = __float2bfloat16_rn(out);
             if (dbg_h) dbg_h[((size_t)b * kProposals + u) * G + j] = out;
         }
     }
@@ -351,8 +346,8 @@ __global__ void __launch_bounds__(kBatchThreads) k_correct_pool_batch(
 }
 
 template <typename T>
-using GruKern = void (*)(const T*, const T*, const T*, const float*, float*, const int32_t*, const int32_t*,
-                         const unsigned long long*, int*, int*, float*, int, int, int, int, int);
+using GruKern = void (*)(const float*, const T*, const float*, float*, __nv_bfloat16*, const int32_t*,
+                         const int32_t*, const unsigned long long*, int*, int*, float*, int, int, int, int);
 template <typename T>
 using Fc1Kern = void (*)(const T*, const float*, const T*, float*, __nv_bfloat16*, float*, int, int, int, int);
 
@@ -404,25 +399,24 @@ bool batch_kernels_supported(const domino_ctx* c) {
     if ((g.E | g.G | g.F) & 7) return false;
     const int mx = g.E > g.G ? (g.E > g.F ? g.E : g.F) : (g.G > g.F ? g.G : g.F);
     if (nch_of(mx) > 8) return false;
-    const size_t gru_smem = (size_t)3 * kJT * (g.E + g.G) * 2;
+    const size_t gru_smem = (size_t)3 * kJT * g.G * 2;
     return gru_smem <= 200 * 1024;
 }
 
-cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u) {
+cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u, __nv_bfloat16* h16_out) {
     using T = __nv_bfloat16;
     const domino_config& g = c->cfg;
     const float* h_in = c->h + (size_t)h_slot(u + 1) * g.max_B * g.G;
     float* h_out = c->h + (size_t)h_slot(u) * g.max_B * g.G;
-    const int mx = g.E > g.G ? g.E : g.G;
-    GruKern<T> kern = pick_gru<T>(nch_of(mx));
-    const size_t smem = (size_t)3 * kJT * (g.E + g.G) * sizeof(T);
+    GruKern<T> kern = pick_gru<T>(nch_of(g.G));
+    const size_t smem = (size_t)3 * kJT * g.G * sizeof(T);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = (g.G + kJT - 1) / kJT;
     ++r.launches;
-    return launch_pdl(kern, dim3(grid), dim3(kBatchThreads), smem, r.st, (const T*)c->emb, (const T*)c->w_ih,
-                      (const T*)c->w_hh, h_in, h_out, r.verified, r.forced, (const unsigned long long*)c->keys, c->bad,
-                      c->err, r.dbg.h, u, r.B, g.V, g.E, g.G);
+    return launch_pdl(kern, dim3(grid), dim3(kBatchThreads), smem, r.st, (const float*)c->gi_table,
+                      (const T*)c->w_hh, h_in, h_out, h16_out, r.verified, r.forced,
+                      (const unsigned long long*)c->keys, c->bad, c->err, r.dbg.h, u, r.B, g.V, g.G);
 }
 
 cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k) {

@@ -203,8 +203,9 @@ __global__ void __launch_bounds__(1024) k_pool_select(const float* __restrict__ 
 // One bias-free GRU update (gate rows r|z|n): one warp per state element j,
 // looping over requests.  u = 0 consumes the verified token with h = 0;
 // u >= 1 consumes proposal u-1 (teacher-forced token when `forced` is set).
+// The input side W_ih emb[t] is row t of the table built at load time.
 template <typename T>
-__global__ void __launch_bounds__(256) k_gru(const T* __restrict__ emb, const T* __restrict__ w_ih,
+__global__ void __launch_bounds__(256) k_gru(const float* __restrict__ gi_table,
                                              const T* __restrict__ w_hh, const float* __restrict__ h_in,
                                              float* __restrict__ h_out, const int32_t* __restrict__ verified,
                                              const int32_t* __restrict__ forced,
@@ -227,10 +228,8 @@ __global__ void __launch_bounds__(256) k_gru(const T* __restrict__ emb, const T*
                 }
                 t = 0;
             }
-            const T* x = emb + (size_t)t * E;
-            float gi_r = warp_dot_tt(w_ih + (size_t)j * E, x, E, lane);
-            float gi_z = warp_dot_tt(w_ih + (size_t)(G + j) * E, x, E, lane);
-            float gi_n = warp_dot_tt(w_ih + (size_t)(2 * G + j) * E, x, E, lane);
+            const float* gi = gi_table + (size_t)t * 3 * G;
+            const float gi_r = gi[j], gi_z = gi[G + j], gi_n = gi[2 * G + j];
             float gh_r = 0.f, gh_z = 0.f, gh_n = 0.f, hp = 0.f;
             if (u > 0) {
                 const float* hv = h_in + (size_t)b * G;
@@ -494,13 +493,12 @@ cudaError_t launch_gru(domino_ctx* c, RunArgs& r, int u) {
     float* h_out = c->h + (size_t)h_slot(u) * g.max_B * g.G;
     int grid = grid_for(8, g.G, c->num_sms * 4);
     if (g.dtype == DOMINO_DTYPE_FP32)
-        k_gru<float><<<grid, 256, 0, r.st>>>((const float*)c->emb, (const float*)c->w_ih, (const float*)c->w_hh,
-                                             h_in, h_out, r.verified, r.forced, c->keys, c->bad, c->err, r.dbg.h,
-                                             u, r.B, g.V, g.E, g.G);
+        k_gru<float><<<grid, 256, 0, r.st>>>(c->gi_table, (const float*)c->w_hh, h_in, h_out, r.verified, r.forced,
+                                             c->keys, c->bad, c->err, r.dbg.h, u, r.B, g.V, g.E, g.G);
     else
-        k_gru<__nv_bfloat16><<<grid, 256, 0, r.st>>>(
-            (const __nv_bfloat16*)c->emb, (const __nv_bfloat16*)c->w_ih, (const __nv_bfloat16*)c->w_hh, h_in, h_out,
-            r.verified, r.forced, c->keys, c->bad, c->err, r.dbg.h, u, r.B, g.V, g.E, g.G);
+        k_gru<__nv_bfloat16><<<grid, 256, 0, r.st>>>(c->gi_table, (const __nv_bfloat16*)c->w_hh, h_in, h_out,
+                                                     r.verified, r.forced, c->keys, c->bad, c->err, r.dbg.h, u, r.B,
+                                                     g.V, g.E, g.G);
     DOMINO_LAUNCH_CHECK();
     return cudaSuccess;
 }

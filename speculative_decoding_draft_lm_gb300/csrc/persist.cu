@@ -46,7 +46,8 @@ constexpr int kMaxSeg = 2048;      // rows (or pool entries) per CTA
 
 template <typename T>
 struct PersistParams {
-    const T *emb, *w_ih, *w_hh, *fc1, *fc2, *bias, *s;
+    const T *w_hh, *fc1, *fc2, *bias, *s;
+    const float* gi_table;  // [V, 3G] input-side GRU pre-activations of every token
     const int32_t *verified, *forced, *pool;
     const float* L;
     float* h;       // [2][max_B*G]
@@ -272,7 +273,7 @@ __host__ __device__ inline int phase_c_requests(int B, int K, int seg) {
 }
 
 struct Layout {
-    int ring, bars, sa, sx, sh, sg, sL, sbias, stot, sbest, stok, misc, total;
+    int ring, bars, sa, sh, sg, sL, sbias, stot, sbest, stok, misc, total;
     __host__ __device__ Layout(int n_slots, int slot_bytes, int E, int G, int F, int seg, int B, int K) {
         auto up = [](int x) { return (x + 127) & ~127; };
         const int nreq = phase_c_requests(B, K, seg), ngru = B < kGruGroup ? B : kGruGroup;
@@ -280,7 +281,6 @@ struct Layout {
         ring = o; o = up(o + n_slots * slot_bytes);
         bars = o; o = up(o + 16 * n_slots);
         sa = o;   o = up(o + 4 * nreq * F);
-        sx = o;   o = up(o + 4 * ngru * E);
         sh = o;   o = up(o + 4 * ngru * G);
         sg = o;   o = up(o + 4 * 9 * kGruGroup * 64);   // gate products + next hidden-side products
         sL = o;   o = up(o + 4 * seg);
@@ -300,7 +300,6 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     uint8_t* ring = sm + lay.ring;
     const uint32_t full0 = tc::smem_u32(sm + lay.bars), empty0 = full0 + 8 * p.n_slots;
     float* sa = reinterpret_cast<float*>(sm + lay.sa);
-    float* sx = reinterpret_cast<float*>(sm + lay.sx);
     float* sh = reinterpret_cast<float*>(sm + lay.sh);
     float* sg = reinterpret_cast<float*>(sm + lay.sg);
     float* sL = reinterpret_cast<float*>(sm + lay.sL);
@@ -442,54 +441,45 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         const bool need_gh = u > 0 && !gh_ready;
         for (int g0 = 0; g0 < B; g0 += kGruGroup) {
             const int ng = min(kGruGroup, B - g0);
-            // first item's weight rows are requested before the staging loads
-            RegRow<T, NCH> wi, wh;
+            // the input side W_ih x of every request is a row of the token table;
+            // only the hidden side W_hh h is contracted here (unless precomputed)
+            RegRow<T, NCH> wh;
             int it = warp;
-            if (it < jn * 3) {
+            if (need_gh && it < jn * 3) {  // first item's weight row before the staging loads
                 const int jj = it / 3, gate = it % 3;
-                wi.load(p.w_ih + (size_t)(gate * G + j0 + jj) * E, E, lane, pol_keep);
-                if (need_gh) wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
+                wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
             }
             cons_sync();  // stok visible
-            for (int i = tid; i < ng * E; i += kConsumerWarps * 32) {
-                const int b = i / E, e = i % E;
-                sx[b * E + e] = to_f32(p.emb[(size_t)stok[g0 + b] * E + e]);
-            }
-            if (u > 0 && !gh_ready)
+            if (need_gh) {
                 for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
                     const int b = i / G, e = i % G;
                     sh[b * G + e] = __ldcg(&h_in[(size_t)(g0 + b) * G + e]);
                 }
-            cons_sync();
-            for (; it < jn * 3; it += kConsumerWarps) {
-                const int jj = it / 3, gate = it % 3;
-                if (it != warp) {
-                    wi.load(p.w_ih + (size_t)(gate * G + j0 + jj) * E, E, lane, pol_keep);
-                    if (need_gh) wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
-                }
+                cons_sync();
+                for (; it < jn * 3; it += kConsumerWarps) {
+                    const int jj = it / 3, gate = it % 3;
+                    if (it != warp) wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
 #pragma unroll
-                for (int b = 0; b < kGruGroup; ++b) {
-                    if (b < ng) {
-                        const float gi = warp_sum(row_dot_smem(wi, sx + b * E, E, lane));
-                        float gh = 0.f;
-                        if (need_gh) gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
-                        else if (u > 0) gh = sgh[((g0 + b) * 64 + jj) * 3 + gate];
-                        if (lane == 0) {
-                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 0] = gi;
-                            sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 1] = gh;
+                    for (int b = 0; b < kGruGroup; ++b) {
+                        if (b < ng) {
+                            const float gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
+                            if (lane == 0) sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 1] = gh;
                         }
                     }
                 }
+                cons_sync();
             }
-            cons_sync();
             for (int i = tid; i < jn * ng; i += kConsumerWarps * 32) {
                 const int jj = i / ng, b = i % ng;
-                const float* gr = sg + ((jj * 3 + 0) * kGruGroup + b) * 2;
-                const float* gz = sg + ((jj * 3 + 1) * kGruGroup + b) * 2;
-                const float* gn = sg + ((jj * 3 + 2) * kGruGroup + b) * 2;
-                const float r = sigmoidf_(gr[0] + gr[1]);
-                const float zg = sigmoidf_(gz[0] + gz[1]);
-                const float n = tanhf(gn[0] + r * gn[1]);
+                const float* gi = p.gi_table + (size_t)stok[g0 + b] * 3 * G + j0 + jj;
+                float gh[3];
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    gh[q] = need_gh ? sg[((jj * 3 + q) * kGruGroup + b) * 2 + 1]
+                                    : (u > 0 ? sgh[((g0 + b) * 64 + jj) * 3 + q] : 0.f);
+                const float r = sigmoidf_(__ldg(gi) + gh[0]);
+                const float zg = sigmoidf_(__ldg(gi + G) + gh[1]);
+                const float n = tanhf(__ldg(gi + 2 * G) + r * gh[2]);
                 const float hp = u > 0 ? sh[b * G + j0 + jj] : 0.f;
                 const float hn = (1.f - zg) * n + zg * hp;
                 h_out[(size_t)(g0 + b) * G + j0 + jj] = hn;
@@ -802,8 +792,7 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     } lay{pl.smem};
 
     PersistParams<T> p;
-    p.emb = (const T*)c->emb;
-    p.w_ih = (const T*)c->w_ih;
+    p.gi_table = c->gi_table;
     p.w_hh = (const T*)c->w_hh;
     p.fc1 = (const T*)c->fc1;
     p.fc2 = (const T*)c->fc2;
