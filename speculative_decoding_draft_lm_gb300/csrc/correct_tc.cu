@@ -26,6 +26,10 @@ namespace {
 
 struct EpiCorrect {
     static constexpr int kScratchWords = tc::kEpiScratch;
+    // A chunks beyond the first ring warmed into L2 before the dependent-launch
+    // wait: fc2 streams while the GRU and projector kernels before it run
+    // (24 chunks of 16 KB per CTA: 58 MB over 152 CTAs, about a fifth of fc2)
+    static constexpr int kL2Ahead = 24;
     const __nv_bfloat16* bias;  // [V]
     const float* L;             // [B,16,V]
     unsigned long long* keys;   // [B,16]

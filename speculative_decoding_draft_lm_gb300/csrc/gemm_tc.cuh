@@ -137,6 +137,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mbar_arrive_expect_tx(full0 + 8 * i, S::STAGE);
                 tma_load_2d(smem_u32(smem + (size_t)i * S::STAGE), ta, kk * kBK, arow, full0 + 8 * i, pol_a);
             }
+            if (Epi::kL2Ahead > 0) {
+                const uint64_t pol_l2 = policy_evict_normal();
+                const int ahead = total < pre + Epi::kL2Ahead ? total : pre + Epi::kL2Ahead;
+                for (int i = pre; i < ahead; ++i) {
+                    const int t = blockIdx.x + (i / k_iters) * gridDim.x, kk = i % k_iters;
+                    const CUtensorMap* ta;
+                    const int arow = a_row(t, ta);
+                    tma_prefetch_2d(ta, kk * kBK, arow, pol_l2);
+                }
+            }
             pdl_wait();
             int stage = 0;
             uint32_t phase = 0;

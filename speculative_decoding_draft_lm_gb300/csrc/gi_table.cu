@@ -20,6 +20,7 @@ namespace {
 
 struct EpiTable {
     static constexpr int kScratchWords = 1;
+    static constexpr int kL2Ahead = 0;
     float* T;  // [V, N]
     int V, N;
     __device__ __forceinline__ void begin(unsigned long long*, int) const {}

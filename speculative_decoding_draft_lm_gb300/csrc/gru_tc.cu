@@ -42,6 +42,7 @@ __global__ void k_pack_gru(const __nv_bfloat16* __restrict__ w_hh, __nv_bfloat16
 
 struct EpiGru {
     static constexpr int kScratchWords = 1;
+    static constexpr int kL2Ahead = 0;
     const float* gi_table;      // [V, 3G]
     const float* h_in;          // [B,G] state before the update
     float* h_out;               // [B,G]
@@ -124,6 +125,7 @@ struct EpiGru {
 
 struct EpiFc1 {
     static constexpr int kScratchWords = 1;
+    static constexpr int kL2Ahead = 0;
     const __nv_bfloat16* s;     // [B,15,F]
     float* a;                   // [B,F]
     __nv_bfloat16* a16;         // [a_rows,F]
@@ -176,16 +178,15 @@ cudaError_t launch_gemm(domino_ctx* c, RunArgs& r, const CUtensorMap& tmA, const
                       c->err);
 }
 
+// 16 requests per tile for both contractions: their A matrices are small
+// (W_hh 8 MB, fc1 2 MB), so a batch spreads over ceil(B/16) times as many
+// CTAs, each with a short epilogue, and re-reads A from L2.
+constexpr int kGruBN = 16;
+
 template <class Epi>
 cudaError_t launch_any_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int K,
                           const Epi& epi) {
-    switch (correct_bn(r.B)) {
-        case 16: return launch_gemm<16>(c, r, tmA, tmB, M, K, epi);
-        case 32: return launch_gemm<32>(c, r, tmA, tmB, M, K, epi);
-        case 64: return launch_gemm<64>(c, r, tmA, tmB, M, K, epi);
-        case 128: return launch_gemm<128>(c, r, tmA, tmB, M, K, epi);
-        default: return launch_gemm<256>(c, r, tmA, tmB, M, K, epi);
-    }
+    return launch_gemm<kGruBN>(c, r, tmA, tmB, M, K, epi);
 }
 
 }  // namespace
@@ -217,7 +218,7 @@ cudaError_t pack_gru_weights(domino_ctx* c, cudaStream_t st) {
 
 cudaError_t prepare_gru_tc(domino_ctx* c, RunArgs& r, GruMaps* m) {
     const domino_config& g = c->cfg;
-    const uint32_t bn = (uint32_t)correct_bn(r.B);
+    const uint32_t bn = (uint32_t)kGruBN;  // box rows = the contractions' N tile
     for (int i = 0; i < 2; ++i) {
         cudaError_t e = make_tmap_bf16(&m->h[i], c->h16 + (size_t)i * c->a_rows * g.G, (uint64_t)c->a_rows,
                                        (uint64_t)g.G, bn);
