@@ -30,6 +30,7 @@ struct EpiCorrect {
     // wait: fc2 streams while the GRU and projector kernels before it run
     // (24 chunks of 16 KB per CTA: 58 MB over 152 CTAs, about a fifth of fc2)
     static constexpr int kL2Ahead = 24;
+    static constexpr int kPfChunk = 17;  // prefetch registers per 16-column chunk
     const __nv_bfloat16* bias;  // [V]
     const float* L;             // [B,16,V]
     unsigned long long* keys;   // [B,16]
@@ -44,13 +45,30 @@ struct EpiCorrect {
         for (int b = t; b < n; b += tc::kEpiThreads)
             if (sb[b]) atomicMax(&keys[(size_t)b * kBlock + k], sb[b]);
     }
-    // base logits of the tile's first PF requests for this thread's row
+    // per 16-column chunk: the base logits of its requests for this thread's
+    // row, and (lane j < 16) the pool-membership word of request j for the
+    // warp's 32 rows, kept as raw bits
     template <int PF>
     __device__ __forceinline__ void prefetch(int col0, int row, float* pf) const {
         const bool ok = row < V;
 #pragma unroll
-        for (int j = 0; j < PF; ++j)
-            pf[j] = (ok && col0 + j < B) ? __ldg(&L[((size_t)(col0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
+        for (int cc = 0; cc < PF / kPfChunk; ++cc) {
+            float* p = pf + cc * kPfChunk;
+            const int c0 = col0 + 16 * cc;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                p[j] = (ok && c0 + j < B) ? __ldg(&L[((size_t)(c0 + j) * kBlock + kRowOffset + k) * V + row]) : 0.f;
+            p[16] = __uint_as_float(mask_word(c0, row));
+        }
+    }
+    // lane j < 16: membership bits of request col0 + j for the warp's rows
+    // (row & ~31) .. +31; the word exists while the warp's first row is below
+    // V, even when this lane's own row is past it
+    __device__ __forceinline__ uint32_t mask_word(int col0, int row) const {
+        const int j = row & 31;
+        return (mask && j < 16 && col0 + j < B && (row >> 5) < mask_words)
+                   ? __ldg(&mask[(size_t)(col0 + j) * mask_words + (row >> 5)])
+                   : 0u;
     }
     __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane,
                                                unsigned long long* sb, const float* pf) const {
@@ -68,12 +86,11 @@ struct EpiCorrect {
         }
         const float bv = ok ? __bfloat162float(bias[row]) : 0.f;
         uint32_t member = 0xffffu;  // bit j: column j may take this row
-        if (mask && ok) {
+        if (mask) {  // uniform: every lane takes part in the shuffles
+            const uint32_t w = pf ? __float_as_uint(pf[16]) : mask_word(col0, row);
             member = 0u;
-            const uint32_t* mw = mask + (size_t)col0 * mask_words + (row >> 5);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                if (j < nb) member |= ((__ldg(mw + (size_t)j * mask_words) >> (row & 31)) & 1u) << j;
+            for (int j = 0; j < 16; ++j) member |= ((__shfl_sync(0xffffffffu, w, j) >> (row & 31)) & 1u) << j;
         }
         unsigned long long kk[16];
 #pragma unroll

@@ -13,7 +13,7 @@
 //               so that a wide tile's epilogue keeps pace with its MMAs
 //
 // Epi provides begin(scratch, t) / prefetch(col0, row, pf) /
-// operator()(col0, row, v[16], lane, scratch, pf + 16c) / end(scratch, t),
+// operator()(col0, row, v[16], lane, scratch, pf + Epi::kPfChunk * c) / end(scratch, t),
 // t = epilogue thread 0..kEpiThreads-1; `scratch` is Epi::kScratchWords per-block
 // 64-bit words in shared memory (per-request argmax words); operator() must
 // not wait on the other epilogue warps (after a timed-out wait they may have
@@ -233,7 +233,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t acc_phase = 0;
         epi.begin(scratch, et);
         epi_bar();
-        constexpr int PF = 16 * HC < kPrefetch ? 16 * HC : kPrefetch;
+        // Epi::kPfChunk prefetch registers per 16-column chunk, for the
+        // first kPrefetch / 16 chunks of this half
+        constexpr int PFC = Epi::kPfChunk;
+        constexpr int PF_CHUNKS = HC < kPrefetch / 16 ? HC : kPrefetch / 16;
+        constexpr int PF = PFC * PF_CHUNKS;
         float pf[PF];
         if ((int)blockIdx.x < tiles && c_lo < c_hi) {
             const int t0 = blockIdx.x;
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (c < c_hi) {  // uniform over the warp
                     float v[16];
                     tmem_ld16(tbase + 16 * c, v);
-                    epi(n * BN + 16 * c, row, v, lane, scratch, 16 * i < PF ? pf + 16 * i : nullptr);
+                    epi(n * BN + 16 * c, row, v, lane, scratch, i < PF_CHUNKS ? pf + PFC * i : nullptr);
                 }
             }
             const int tn = t + gridDim.x;  // the next tile's epilogue inputs, during its MMAs

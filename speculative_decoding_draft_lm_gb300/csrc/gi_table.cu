@@ -21,6 +21,7 @@ namespace {
 struct EpiTable {
     static constexpr int kScratchWords = 1;
     static constexpr int kL2Ahead = 0;
+    static constexpr int kPfChunk = 16;  // prefetch registers per 16-column chunk
     float* T;  // [V, N]
     int V, N;
     __device__ __forceinline__ void begin(unsigned long long*, int) const {}

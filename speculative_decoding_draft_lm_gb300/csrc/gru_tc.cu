@@ -43,6 +43,7 @@ __global__ void k_pack_gru(const __nv_bfloat16* __restrict__ w_hh, __nv_bfloat16
 struct EpiGru {
     static constexpr int kScratchWords = 1;
     static constexpr int kL2Ahead = 0;
+    static constexpr int kPfChunk = 16;  // prefetch registers per 16-column chunk
     const float* gi_table;      // [V, 3G]
     const float* h_in;          // [B,G] state before the update
     float* h_out;               // [B,G]
@@ -126,6 +127,7 @@ struct EpiGru {
 struct EpiFc1 {
     static constexpr int kScratchWords = 1;
     static constexpr int kL2Ahead = 0;
+    static constexpr int kPfChunk = 16;  // prefetch registers per 16-column chunk
     const __nv_bfloat16* s;     // [B,15,F]
     float* a;                   // [B,F]
     __nv_bfloat16* a16;         // [a_rows,F]

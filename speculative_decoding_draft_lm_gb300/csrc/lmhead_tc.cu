@@ -31,6 +31,7 @@ namespace {
 struct EpiLmHead {
     static constexpr int kScratchWords = tc::kEpiScratch;
     static constexpr int kL2Ahead = 0;
+    static constexpr int kPfChunk = 16;  // prefetch registers per 16-column chunk
     float* L;                  // [B,16,V]
     unsigned long long* keys;  // [B,16], slot 0 = p_1
     float* score;              // [B,V] or null
