@@ -600,13 +600,17 @@ def read_traffic(kernel: str, workload: str):
 
 
 def source_hash() -> str:
+    """Hash of the kernel sources with // comments and blank lines dropped, so
+    that a comment edit does not orphan the committed counters."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_draft_lm_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in fh]
+            h.update(f.encode() + b"\0" + "\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()[:16]
 
 

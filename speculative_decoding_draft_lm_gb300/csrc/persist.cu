@@ -1,6 +1,7 @@
 // Persistent single-launch driver of the rollout after the LM-head: the two
-// GRU seed updates and the 14 dependent corrected steps run in one
-// cooperative kernel (one CTA per SM) separated by software grid barriers.
+// GRU seed updates and the 14 dependent corrected steps (fewer with an early
+// stop) run in one cooperative kernel (one CTA per SM) separated by software
+// grid barriers.
 //
 // Per corrected step k (page "Add correctness-first Domino support to DFlash
 // V2", section "Design"; page "[Spec] Add Domino projector support to DFlash
@@ -11,7 +12,9 @@
 //            contiguous slice of fc2 rows (full vocabulary) or of the pool
 //            entries; per-CTA best folded into the step's argmax word
 //   -- grid barrier --
-//   phase A  h = GRU(emb[p_{k+1}], h)      each CTA: a slice of the G outputs
+//   phase A  h = GRU(emb[p_{k+1}], h)      each CTA: a slice of the G outputs;
+//            the input side W_ih emb[p] is a row of the token table built at
+//            load time, the hidden side W_hh h is computed during phase C
 //   -- grid barrier --
 //
 // A producer warp streams the fc2 rows (contiguous slices, or one row per
@@ -21,10 +24,12 @@
 // the ring refills.  Successive steps walk the slice in opposite directions,
 // so a step starts on the rows the previous one read last (still in L2).
 //
-// The correction here runs on CUDA cores (one warp per row, fp32 FMA), which
-// suits one request per row: B = 1 over the full vocabulary, or pool entries
-// of any request.  Every wait (grid barrier, ring slot) is bounded; on a
-// timeout the kernel raises the device error word and returns.
+// The correction here runs on CUDA cores (a consumer warp takes a whole
+// 4-row slot and keeps the activations in registers, fp32 FMA; row totals go
+// to shared memory and an epilogue adds bias and base logits and takes the
+// argmax), which suits one request per row: B = 1 over the full vocabulary,
+// or pool entries of any request.  Every wait (grid barrier, ring slot) is
+// bounded; on a timeout the kernel raises the device error word and returns.
 #include "internal.h"
 #include "tc_common.cuh"
 
