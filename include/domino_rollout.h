@@ -102,7 +102,10 @@ DOMINO_API int domino_rollout_load_weights(domino_ctx* ctx, const void* lm_head,
 DOMINO_API int domino_rollout_load_backbone_proj(domino_ctx* ctx, const void* w_hid);
 
 /* Run one block rollout for B requests on `cuda_stream` (a cudaStream_t,
- * NULL = legacy default stream).  DEVICE pointers, owned by the caller:
+ * NULL = legacy default stream).  Asynchronous, with no host
+ * synchronisation: after one ordinary call with the same B and K (which sets
+ * kernel attributes once), a call can be captured into a CUDA graph and the
+ * graph replayed with new contents in the same input buffers.  DEVICE pointers, owned by the caller:
  *   hidden       [B,16,H]  draft hidden states (config dtype, 16-B aligned)
  *   s            [B,15,F]  per-step additive term of projector layer 1
  *                          (row 0 is not read; row k serves corrected step k);
