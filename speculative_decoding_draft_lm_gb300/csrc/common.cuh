@@ -147,23 +147,6 @@ __device__ __forceinline__ float warp_dot(const T* __restrict__ w, const float* 
     }
     return warp_sum(acc);
 }
-// Same, with the vector in the weight dtype (e.g. an embedding row).
-template <typename T>
-__device__ __forceinline__ float warp_dot_tt(const T* __restrict__ w, const T* __restrict__ x, int n, int lane) {
-    float acc = 0.f;
-    if ((n & 7) == 0) {
-        for (int i = lane * 8; i < n; i += 256) {
-            float e[8], f[8];
-            load8(w + i, e);
-            load8(x + i, f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc = fmaf(e[j], f[j], acc);
-        }
-    } else {
-        for (int i = lane; i < n; i += 32) acc = fmaf(to_f32(w[i]), to_f32(x[i]), acc);
-    }
-    return warp_sum(acc);
-}
 
 }  // namespace domino
 

@@ -26,16 +26,6 @@ constexpr int kBatchThreads = 256;
 template <typename T, int NCH>
 struct VecRegs {
     float v[NCH][8];
-    __device__ __forceinline__ void load_t(const T* p, int n, int lane) {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int e = (lane + 32 * c) * 8;
-            if (e < n) load8(p + e, v[c]);
-            else
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[c][i] = 0.f;
-        }
-    }
     __device__ __forceinline__ void load_f(const float* p, int n, int lane) {
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
@@ -137,6 +127,16 @@ __global__ void __launch_bounds__(kBatchThreads) k_gru_batch(
             }
             t = 0;
         }
+        // the token's input-side values, requested before the hidden-side products
+        const int j = j0 + lane;
+        const float* gi = gi_table + (size_t)t * 3 * G;
+        float gir = 0.f, giz = 0.f, gin = 0.f, hp = 0.f;
+        if (lane < jn) {
+            gir = __ldg(gi + j);
+            giz = __ldg(gi + G + j);
+            gin = __ldg(gi + 2 * G + j);
+            if (u > 0) hp = h_in[(size_t)b * G + j];
+        }
         float gh[3 * kJT];
 #pragma unroll
         for (int i = 0; i < 3 * kJT; ++i) gh[i] = 0.f;
@@ -154,12 +154,9 @@ __global__ void __launch_bounds__(kBatchThreads) k_gru_batch(
                 if (jj == lane) {
                     hr = gh[0 * kJT + jj]; hz = gh[1 * kJT + jj]; hn = gh[2 * kJT + jj];
                 }
-            const int j = j0 + lane;
-            const float* gi = gi_table + (size_t)t * 3 * G;
-            const float r = sigmoidf_(gi[j] + hr);
-            const float zg = sigmoidf_(gi[G + j] + hz);
-            const float n = tanhf(gi[2 * G + j] + r * hn);
-            const float hp = u > 0 ? h_in[(size_t)b * G + j] : 0.f;
+            const float r = sigmoidf_(gir + hr);
+            const float zg = sigmoidf_(giz + hz);
+            const float n = tanhf(gin + r * hn);
             const float out = (1.f - zg) * n + zg * hp;
             h_out[(size_t)b * G + j] = out;
             if (h16_out) h16_out[(size_t)b * G + j] = __float2bfloat16_rn(out);

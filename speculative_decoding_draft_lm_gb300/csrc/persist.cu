@@ -193,64 +193,6 @@ __device__ __forceinline__ float row_dot_smem(const RegRow<T, NCH>& w, const flo
     return a0 + a1;
 }
 
-// Two independent fp32 FMAs in one instruction (round to nearest, like fmaf).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    unsigned long long A, Bv, C, D;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(Bv) : "f"(b.x), "f"(b.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(c.x), "f"(c.y));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(Bv), "l"(C));
-    float2 d;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(D));
-    return d;
-}
-// 8 elements of a shared-memory row as 4 (even, odd) pairs
-__device__ __forceinline__ void lds_pairs(const __nv_bfloat16* p, float2* o) {
-    const uint4 q = *reinterpret_cast<const uint4*>(p);
-    o[0] = make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u));
-    o[1] = make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
-    o[2] = make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u));
-    o[3] = make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
-}
-__device__ __forceinline__ void lds_pairs(const float* p, float2* o) {
-    const float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
-    o[0] = make_float2(x.x, x.y);
-    o[1] = make_float2(x.z, x.w);
-    o[2] = make_float2(y.x, y.y);
-    o[3] = make_float2(y.z, y.w);
-}
-
-// 16-byte chunk of 8 row elements held in registers
-template <typename T>
-struct ChunkOf;
-template <>
-struct ChunkOf<__nv_bfloat16> {
-    using type = uint4;
-    __device__ __forceinline__ static uint4 load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint4*>(p); }
-    __device__ __forceinline__ static void pairs(const uint4& q, float2* o) {
-        o[0] = make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u));
-        o[1] = make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
-        o[2] = make_float2(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u));
-        o[3] = make_float2(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u));
-    }
-};
-struct F8 {
-    float4 a, b;
-};
-template <>
-struct ChunkOf<float> {
-    using type = F8;
-    __device__ __forceinline__ static F8 load(const float* p) {
-        return F8{reinterpret_cast<const float4*>(p)[0], reinterpret_cast<const float4*>(p)[1]};
-    }
-    __device__ __forceinline__ static void pairs(const F8& q, float2* o) {
-        o[0] = make_float2(q.a.x, q.a.y);
-        o[1] = make_float2(q.a.z, q.a.w);
-        o[2] = make_float2(q.b.x, q.b.y);
-        o[3] = make_float2(q.b.z, q.b.w);
-    }
-};
-
 // Sum each of 4 per-lane values over the warp with 6 shuffles (a transposed
 // butterfly).  Lane l ends with the total of value ((l >> 4) & 1) * 2 +
 // ((l >> 3) & 1).
