@@ -73,18 +73,26 @@ typedef struct {
     int dtype;   /* DOMINO_DTYPE_* */
 } domino_config;
 
-/* Create a context on CUDA device `device` and allocate its workspace there:
- * base logits [max_B,16,V] fp32, pool scores [max_B,V], pool [max_B,max_K],
- * GRU/projector state and the per-step argmax words.  *out receives the
- * context (NULL on failure).  Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM. */
+/* Create a context on CUDA device `device` and allocate its workspace there
+ * in one allocation: base logits [max_B,16,V] fp32, pool scores [max_B,V],
+ * pool [max_B,max_K], GRU/projector state, the per-step argmax words, and the
+ * token table [V,3G] fp32 that load_weights fills (1.9 GB at V = 151,936,
+ * G = 1024).  *out receives the context (NULL on failure).
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM. */
 DOMINO_API int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device);
 
 /* Register the weights: DEVICE pointers, row-major, in the config's dtype,
  * BORROWED (the caller keeps them alive and unchanged until destroy or the
  * next load_weights).  Shapes: lm_head [V,H]; emb [V,E]; w_ih [3G,E] and
  * w_hh [3G,G] with gate rows r|z|n; fc1 [F,G]; fc2 [V,F]; bias [V].
- * Pointers must be 16-byte aligned.  Builds the TMA descriptors; no copy.
- * Errors: INVALID_ARG, CUDA. */
+ * Pointers must be 16-byte aligned.  Builds the TMA descriptors and derives,
+ * on the legacy default stream and synchronously, the context's own copies:
+ * the input-side GRU pre-activations of every token, T[v] = w_ih . emb[v]
+ * (page "Add correctness-first Domino support to DFlash V2", section
+ * "Design": the GRU consumes the embedding of the realised token, so this
+ * half depends on the token alone), and for bf16 a packed w_hh for the
+ * tensor-core GRU.  Changing emb, w_ih or w_hh afterwards requires calling
+ * load_weights again.  Errors: INVALID_ARG, CUDA. */
 DOMINO_API int domino_rollout_load_weights(domino_ctx* ctx, const void* lm_head, const void* emb,
                                 const void* w_ih, const void* w_hh, const void* fc1,
                                 const void* fc2, const void* bias);
