@@ -436,6 +436,24 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         }
     };
 
+    // ---- W_hh h_k of the next GRU update (one request group, h_k staged in
+    // sh by the projector phase of step k), into sgh
+    auto hidden_products = [&](int k) {
+        if (!(pre_gh && k < p.n_corr) || *abort_flag) return;
+        for (int it = warp; it < jn * 3; it += kConsumerWarps) {
+            const int jj = it / 3, gate = it % 3;
+            RegRow<T, NCH> wh;
+            wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
+#pragma unroll
+            for (int b = 0; b < kGruGroup; ++b) {
+                if (b < B) {
+                    const float gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
+                    if (lane == 0) sgh[(b * 64 + jj) * 3 + gate] = gh;
+                }
+            }
+        }
+    };
+
     // ---- projector layer 1 + SiLU for step k; writes a.  Leaves h_k staged
     // in sh (single group) for the hidden-side GRU products.
     auto fc1 = [&](int k) {
@@ -573,20 +591,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             if (lane == 0) atomicAdd((int*)consumed_ptr, 1);
         }
         // hidden-side GRU products for the next update while the ring refills
-        if (pre_gh && k < p.n_corr && !*abort_flag) {
-            for (int it = warp; it < jn * 3; it += kConsumerWarps) {
-                const int jj = it / 3, gate = it % 3;
-                RegRow<T, NCH> wh;
-                wh.load(p.w_hh + (size_t)(gate * G + j0 + jj) * G, G, lane, pol_keep);
-#pragma unroll
-                for (int b = 0; b < kGruGroup; ++b) {
-                    if (b < B) {
-                        const float gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
-                        if (lane == 0) sgh[(b * 64 + jj) * 3 + gate] = gh;
-                    }
-                }
-            }
-        }
+        hidden_products(k);
         cons_sync();
         // finish every row of the slice: bias, base logit, argmax key
         for (int r = tid; r < nw; r += kConsumerWarps * 32) {

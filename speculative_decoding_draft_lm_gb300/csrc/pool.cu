@@ -5,7 +5,9 @@
 //   score[b, v] = max_{i=1..15} L[b, i, v],
 // ties at the cutoff to the lower id, stored in ascending id order.
 //
-// One thread-block cluster of kRanks CTAs per request.  Each CTA caches its
+// One thread-block cluster of R CTAs per request (R = 16, a non-portable
+// cluster size, for a single row; else 8: at B = 8 eight clusters of 16
+// measured slower than eight of 8, 51 us against 32 us).  Each CTA caches its
 // contiguous slice of the vocabulary as 32-bit orderable keys in shared
 // memory.  An exact radix select over three digit passes (11, 11, 10 bits)
 // finds the K-th largest key T: each pass builds per-CTA histograms with
@@ -35,13 +37,15 @@ namespace domino {
 
 namespace {
 
-constexpr int kRanks = 8;          // CTAs per request (portable cluster size)
+constexpr int kRanksPortable = 8;  // CTAs per request (portable cluster size)
+constexpr int kRanksWide = 16;     // non-portable cluster size for small batches
 constexpr int kPoolThreads = 1024;
 constexpr int kBins = 2048;
 
+template <int R>
 struct PoolShared {
     unsigned hist[kBins];
-    unsigned merged[kBins / kRanks];
+    unsigned merged[kBins / R];
     unsigned warp_tot[32];
     unsigned total;          // this CTA's merged-bin total / block scan total
     unsigned gt, eq;         // compaction counts of this CTA
@@ -80,13 +84,14 @@ __device__ __forceinline__ unsigned block_scan_excl(unsigned x, unsigned* warp_t
 //               writing vocabulary ids to pool[b*out_stride + p*K + j];
 // cand != null: (shards == 1) select among the V candidates cand[b*V + i] (id -1 = none) by
 //               score[b*stride + id], writing the candidate ids to pool[b*out_stride + j].
+template <int R>
 __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* __restrict__ score, long long stride,
                                                                  const int32_t* __restrict__ cand, int shards,
                                                                  int shard_len, int32_t* __restrict__ pool,
                                                                  int out_stride, int V, int K, int chunk) {
     extern __shared__ __align__(16) uint8_t smem[];
-    PoolShared& S = *reinterpret_cast<PoolShared*>(smem);
-    unsigned* keys = reinterpret_cast<unsigned*>(smem + sizeof(PoolShared));
+    PoolShared<R>& S = *reinterpret_cast<PoolShared<R>*>(smem);
+    unsigned* keys = reinterpret_cast<unsigned*>(smem + sizeof(PoolShared<R>));
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = blockIdx.y / shards, shard = blockIdx.y % shards;
@@ -138,12 +143,12 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
         }
         cluster.sync();  // every CTA's histogram is complete
         // this CTA merges the bins [rank*per, (rank+1)*per) of all CTAs
-        const unsigned per = nb / kRanks;
+        const unsigned per = nb / R;
         unsigned mine = 0;
         for (unsigned t = threadIdx.x; t < per; t += kPoolThreads) {
             unsigned s = 0;
 #pragma unroll
-            for (int r = 0; r < kRanks; ++r) s += cluster.map_shared_rank(S.hist, r)[rank * per + t];
+            for (int r = 0; r < R; ++r) s += cluster.map_shared_rank(S.hist, r)[rank * per + t];
             S.merged[t] = s;
             mine += s;
         }
@@ -161,19 +166,19 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
         // `remaining`, then in the highest bin of that slice that does: one
         // warp scans the slice totals and the slice's bins in parallel
         if (threadIdx.x < 32) {
-            const unsigned t = lane < kRanks ? *cluster.map_shared_rank(&S.total, lane) : 0u;
-            unsigned suf = t;  // inclusive suffix over ranks lane..kRanks-1
+            const unsigned t = lane < R ? *cluster.map_shared_rank(&S.total, lane) : 0u;
+            unsigned suf = t;  // inclusive suffix over ranks lane..R-1
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const unsigned y = __shfl_down_sync(0xffffffffu, suf, o);
                 if (lane + o < 32) suf += y;
             }
-            const unsigned hit = __ballot_sync(0xffffffffu, lane < kRanks && suf >= remaining);
-            const int R = 31 - __clz(hit);  // highest rank whose suffix reaches `remaining`
-            const unsigned above = __shfl_sync(0xffffffffu, suf, R) - __shfl_sync(0xffffffffu, t, R);
+            const unsigned hit = __ballot_sync(0xffffffffu, lane < R && suf >= remaining);
+            const int hr = 31 - __clz(hit);  // highest rank whose suffix reaches `remaining`
+            const unsigned above = __shfl_sync(0xffffffffu, suf, hr) - __shfl_sync(0xffffffffu, t, hr);
             const unsigned rem = remaining - above;
-            const unsigned* mg = cluster.map_shared_rank(S.merged, R);
-            const int ppl = (int)per / 32;  // bins per lane (8 or 4)
+            const unsigned* mg = cluster.map_shared_rank(S.merged, hr);
+            const int ppl = (int)per / 32;  // bins per lane (8, 4 or 2)
             unsigned vals[8];
             unsigned lsum = 0;
 #pragma unroll
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
                     const unsigned before = acc;  // keys in bins above bin (lane*ppl + i)
                     acc += vals[i];
                     if (before < rem && acc >= rem) {
-                        S.digit = (unsigned)R * per + (unsigned)(lane * ppl + i);
+                        S.digit = (unsigned)hr * per + (unsigned)(lane * ppl + i);
                         S.rem = rem - before;
                     }
                 }
@@ -250,29 +255,48 @@ __global__ void __launch_bounds__(kPoolThreads, 1) k_pool_cluster(const float* _
 
 namespace {
 
-cudaError_t launch_rows(const float* score, long long stride, const int32_t* cand, int shards, int shard_len,
-                        int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st) {
-    const int chunk = (shard_len + kRanks - 1) / kRanks;
-    const size_t smem = sizeof(PoolShared) + (size_t)chunk * 4;
-    cudaError_t e = cudaFuncSetAttribute(k_pool_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int R>
+cudaError_t launch_rows_r(const float* score, long long stride, const int32_t* cand, int shards, int shard_len,
+                          int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st) {
+    const int chunk = (shard_len + R - 1) / R;
+    const size_t smem = sizeof(PoolShared<R>) + (size_t)chunk * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_pool_cluster<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    if (R > kRanksPortable) {
+        e = cudaFuncSetAttribute(k_pool_cluster<R>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kRanks, B * shards);
+    cfg.gridDim = dim3(R, B * shards);
     cfg.blockDim = dim3(kPoolThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kRanks;
+    attr[0].val.clusterDim.x = R;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_pool_cluster, score, stride, cand, shards, shard_len, pool, out_stride, V, K,
+    return cudaLaunchKernelEx(&cfg, k_pool_cluster<R>, score, stride, cand, shards, shard_len, pool, out_stride, V, K,
                               chunk);
 }
 
-bool fits(int row_len) { return sizeof(PoolShared) + (size_t)((row_len + kRanks - 1) / kRanks) * 4 <= 220 * 1024; }
+// R = 16 for a single row when the GPU has room for it (num_sms = 0: never)
+cudaError_t launch_rows(const float* score, long long stride, const int32_t* cand, int shards, int shard_len,
+                        int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st, int num_sms = 0) {
+    if (num_sms >= kRanksWide && B * shards == 1) {
+        cudaError_t e = launch_rows_r<kRanksWide>(score, stride, cand, shards, shard_len, pool, out_stride, B, V, K, st);
+        if (e == cudaSuccess) return e;
+        cudaGetLastError();  // wide clusters unavailable: the portable size
+    }
+    return launch_rows_r<kRanksPortable>(score, stride, cand, shards, shard_len, pool, out_stride, B, V, K, st);
+}
+
+bool fits(int row_len) {
+    return sizeof(PoolShared<kRanksPortable>) + (size_t)((row_len + kRanksPortable - 1) / kRanksPortable) * 4 <=
+           220 * 1024;
+}
 
 }  // namespace
 
@@ -287,7 +311,7 @@ bool pool_cluster_supported(const domino_ctx* c) { return fits(c->cfg.V); }
 
 cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r) {
     ++r.launches;
-    return launch_rows(c->score, c->cfg.V, nullptr, 1, c->cfg.V, c->pool, r.K, r.B, c->cfg.V, r.K, r.st);
+    return launch_rows(c->score, c->cfg.V, nullptr, 1, c->cfg.V, c->pool, r.K, r.B, c->cfg.V, r.K, r.st, c->num_sms);
 }
 
 bool pool_compact_supported(const domino_ctx* c, int P, int K) {
@@ -300,11 +324,11 @@ cudaError_t launch_pool_compact(domino_ctx* c, RunArgs& r, int P) {
     const int S = (V + P - 1) / P;
     // pass 1: shard-local top-K of every (request, shard) into cand [B, P*K]
     ++r.launches;
-    cudaError_t e = launch_rows(c->score, V, nullptr, P, S, c->cand, P * K, r.B, V, K, r.st);
+    cudaError_t e = launch_rows(c->score, V, nullptr, P, S, c->cand, P * K, r.B, V, K, r.st, c->num_sms);
     if (e != cudaSuccess) return e;
     // pass 2: the global top-K among each request's P*K candidates
     ++r.launches;
-    return launch_rows(c->score, V, c->cand, 1, P * K, c->pool, K, r.B, P * K, K, r.st);
+    return launch_rows(c->score, V, c->cand, 1, P * K, c->pool, K, r.B, P * K, K, r.st, c->num_sms);
 }
 
 }  // namespace domino
