@@ -46,6 +46,11 @@ def test_strerror_and_null_handles(lib):
     assert lib.domino_rollout_run(None, None, None, None, 1, 0, None, None) == R.DOMINO_ERR_INVALID_ARG
     assert lib.domino_rollout_status(None, None) == R.DOMINO_ERR_INVALID_ARG
     assert lib.domino_rollout_set_driver(None, 0) == R.DOMINO_ERR_INVALID_ARG
+    assert lib.domino_rollout_set_proposals(None, 7) == R.DOMINO_ERR_INVALID_ARG
+    assert lib.domino_rollout_set_vocab_partitions(None, 2) == R.DOMINO_ERR_INVALID_ARG
+    assert lib.domino_rollout_load_backbone_proj(None, None) == R.DOMINO_ERR_INVALID_ARG
+    assert lib.domino_rollout_enable_timing(None, 1) == R.DOMINO_ERR_INVALID_ARG
+    assert lib.domino_candidate_pool_static(None, 1, 10, 2, None, None) == R.DOMINO_ERR_INVALID_ARG
     lib.domino_rollout_destroy(None)
     assert lib.domino_rollout_last_launch_count(None) == 0
 
