@@ -223,6 +223,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oWp = take(gru_tc ? (size_t)4 * gru_padded_units(g.G) * g.G * 2 : 0);
     size_t oX = take(gru_tc ? (size_t)2 * c->a_rows * g.G * 2 : 0);
     size_t oT = take((size_t)g.V * 3 * g.G * sizeof(float));
+    size_t oGh = take((size_t)4 * 3 * g.G * sizeof(float));
     const bool pmask = g.max_K > 0 && g.dtype == DOMINO_DTYPE_BF16;
     size_t oM = take(pmask ? (size_t)g.max_B * pool_mask_words(g.V) * 4 : 0);
     size_t oC = take(g.max_K > 0 ? (size_t)g.max_B * DOMINO_MAX_VOCAB_PARTITIONS * g.max_K * 4 : 0);
@@ -247,6 +248,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->wp = gru_tc ? (__nv_bfloat16*)(base + oWp) : nullptr;
     c->h16 = gru_tc ? (__nv_bfloat16*)(base + oX) : nullptr;
     c->gi_table = (float*)(base + oT);
+    c->gh_next = (float*)(base + oGh);
     c->pmask = pmask ? (uint32_t*)(base + oM) : nullptr;
     c->cand = g.max_K > 0 ? (int32_t*)(base + oC) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)

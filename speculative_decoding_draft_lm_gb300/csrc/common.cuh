@@ -180,6 +180,7 @@ struct domino_ctx {
     int* err;                 // device error word
     unsigned int* sync;       // grid-barrier words for the persistent driver
     float* gi_table;          // [V, 3G] input-side GRU pre-activations of every token (built at load)
+    float* gh_next;           // [4][3G] hidden-side pre-activations of the next GRU update (persistent driver)
     __nv_bfloat16* wp;        // [4*Gp, G] packed hidden-side GRU weights (bf16 batches), or null
     __nv_bfloat16* h16;       // [2][a_rows, G] bf16 copies of the GRU state (tensor-core operands)
     void* ws_base;            // single workspace allocation

@@ -56,6 +56,7 @@ struct PersistParams {
     const int32_t *verified, *forced, *pool;
     const float* L;
     float* h;       // [2][max_B*G]
+    float* gh;      // [kGruGroup][3][G] W_hh h of the next update, all units
     float* a;       // [max_B*F]
     unsigned long long* keys;
     int *bad, *err;
@@ -363,10 +364,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     // W_hh h of the next GRU update is computed during the correction phase
     // (its warps have slack while fc2 streams) when all requests fit one group
     const bool pre_gh = B <= kGruGroup;
-    float* sgh = sg + 6 * kGruGroup * 64;  // [kGruGroup][64][3], after the gate products
 
     // ---- one GRU update u for every request; writes h[slot(u)].  With
-    // gh_ready, the hidden-side products are in sgh and h_in is still staged
+    // gh_ready, the hidden-side products are in p.gh and h_in is still staged
     // in sh (it was staged for the projector of the same step).
     auto gru = [&](int u, bool gh_ready) {
         const float* h_in = p.h + (size_t)h_slot(u + 1) * p.max_B * G;
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
 #pragma unroll
                 for (int q = 0; q < 3; ++q)
                     gh[q] = need_gh ? sg[((jj * 3 + q) * kGruGroup + b) * 2 + 1]
-                                    : (u > 0 ? sgh[((g0 + b) * 64 + jj) * 3 + q] : 0.f);
+                                    : (u > 0 ? p.gh[((size_t)(g0 + b) * 3 + q) * G + j0 + jj] : 0.f);
                 const float r = sigmoidf_(__ldg(gi) + gh[0]);
                 const float zg = sigmoidf_(__ldg(gi + G) + gh[1]);
                 const float n = tanhf(__ldg(gi + 2 * G) + r * gh[2]);
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     };
 
     // ---- W_hh h_k of the next GRU update (one request group, h_k staged in
-    // sh by the projector phase of step k), into sgh
+    // sh by the projector phase of step k): this CTA's units, into p.gh
     auto hidden_products = [&](int k) {
         if (!(pre_gh && k < p.n_corr) || *abort_flag) return;
         for (int it = warp; it < jn * 3; it += kConsumerWarps) {
@@ -448,25 +448,85 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             for (int b = 0; b < kGruGroup; ++b) {
                 if (b < B) {
                     const float gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
-                    if (lane == 0) sgh[(b * 64 + jj) * 3 + gate] = gh;
+                    if (lane == 0) p.gh[((size_t)b * 3 + gate) * G + j0 + jj] = gh;
                 }
             }
         }
     };
 
+    // ---- GRU update u for one request group (B <= kGruGroup), computed in
+    // full by every CTA from the token table row, the hidden-side products
+    // p.gh (written by all CTAs during the previous correction) and h_{u-1}
+    // (still staged in sh): the new state replaces sh in place and this CTA
+    // publishes its own slice.  Saves the GRU phase and its grid barrier.
+    auto gru_local = [&](int u) {
+        float* h_out = p.h + (size_t)h_slot(u) * p.max_B * G;
+        if (tid < B) {
+            int t = p.forced ? p.forced[(size_t)tid * kProposals + (u - 1)]
+                             : (int)key_index(__ldcg(&p.keys[(size_t)tid * kBlock + (u - 1)]));
+            if (t < 0 || t >= V) {
+                if (blockIdx.x == 0) {
+                    p.bad[tid] = 1;
+                    atomicOr(p.err, kErrBadToken);
+                }
+                t = 0;
+            }
+            stok[tid] = t;
+        }
+        cons_sync();
+        constexpr int kNT = kConsumerWarps * 32, kPer = 2;  // elements a thread keeps in flight
+        for (int base = 0; base < B * G; base += kPer * kNT) {
+            float in[kPer][6];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {  // every load of the round before any use
+                const int i = base + e * kNT + tid;
+                if (i < B * G) {
+                    const int b = i / G, j = i % G;
+                    const float* gi = p.gi_table + (size_t)stok[b] * 3 * G + j;
+                    const float* gh = p.gh + (size_t)b * 3 * G + j;
+                    in[e][0] = __ldg(gi);
+                    in[e][1] = __ldg(gi + G);
+                    in[e][2] = __ldg(gi + 2 * G);
+                    in[e][3] = __ldcg(gh);
+                    in[e][4] = __ldcg(gh + G);
+                    in[e][5] = __ldcg(gh + 2 * G);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                const int i = base + e * kNT + tid;
+                if (i < B * G) {
+                    const int b = i / G, j = i % G;
+                    const float r = sigmoidf_(in[e][0] + in[e][3]);
+                    const float zg = sigmoidf_(in[e][1] + in[e][4]);
+                    const float n = tanhf(in[e][2] + r * in[e][5]);
+                    const float hn = (1.f - zg) * n + zg * sh[b * G + j];
+                    sh[b * G + j] = hn;
+                    if (j >= j0 && j < j1) {
+                        h_out[(size_t)b * G + j] = hn;
+                        if (p.dbg_h) p.dbg_h[((size_t)b * kProposals + u) * G + j] = hn;
+                    }
+                }
+            }
+        }
+        cons_sync();
+    };
+
     // ---- projector layer 1 + SiLU for step k; writes a.  Leaves h_k staged
     // in sh (single group) for the hidden-side GRU products.
-    auto fc1 = [&](int k) {
+    auto fc1 = [&](int k, bool merged) {
         const float* hv = p.h + (size_t)h_slot(k) * p.max_B * G;
         for (int g0 = 0; g0 < B; g0 += kGruGroup) {
             const int ng = min(kGruGroup, B - g0);
             RegRow<T, NCH> w;
             int f = f0 + warp;
             if (f < f1) w.load(p.fc1 + (size_t)f * G, G, lane, pol_keep);
-            for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
-                const int b = i / G, e = i % G;
-                sh[b * G + e] = __ldcg(&hv[(size_t)(g0 + b) * G + e]);
-            }
+            if (merged) gru_local(k);  // one group: h_k computed into sh, the weight row in flight
+            else
+                for (int i = tid; i < ng * G; i += kConsumerWarps * 32) {
+                    const int b = i / G, e = i % G;
+                    sh[b * G + e] = __ldcg(&hv[(size_t)(g0 + b) * G + e]);
+                }
             cons_sync();
             for (; f < f1; f += kConsumerWarps) {
                 if (f != f0 + warp) w.load(p.fc1 + (size_t)f * G, G, lane, pol_keep);
@@ -656,7 +716,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         stamp();                                                     // 4
         for (int k = 1; k <= p.n_corr; ++k) {                        // 5 + 6 (k-1) + ...
             prefetch_L(k);
-            fc1(k);
+            // one request group: GRU update k joins the projector phase
+            fc1(k, pre_gh && k > 1);
             stamp();                                                 // +0 projector done
             if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
             stamp();                                                 // +1 barrier
@@ -665,10 +726,15 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
             stamp();                                                 // +3 barrier
             if (k < p.n_corr) {
-                gru(k + 1, pre_gh);
-                stamp();                                             // +4 GRU done
-                if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
-                stamp();                                             // +5 barrier
+                if (pre_gh) {  // the next update runs in the next projector phase
+                    stamp();                                         // +4
+                    stamp();                                         // +5
+                } else {
+                    gru(k + 1, false);
+                    stamp();                                         // +4 GRU done
+                    if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+                    stamp();                                         // +5 barrier
+                }
             }
         }
     };
@@ -755,6 +821,7 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     p.pool = c->pool;
     p.L = c->L;
     p.h = c->h;
+    p.gh = c->gh_next;
     p.a = c->a;
     p.keys = c->keys;
     p.bad = c->bad;
