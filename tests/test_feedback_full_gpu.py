@@ -1,0 +1,120 @@
+"""Parity at the real hidden sizes with weights under which the GRU state and
+the projector matter.
+
+With every weight drawn from N(0, 0.02) the GRU state stays near 0.01 and
+fc1 . h near 0.02, at or below the bf16 tolerance, so a GRU or projector that
+produced zeros would still pass the element-wise checks at full size.  Here
+the embedding is N(0, 1), w_ih N(0, 1/E), w_hh N(0, 1/G), fc1 N(0, 1/G) and
+fc2 N(0, 1/F), which keeps |h| of order 0.5 and moves the corrected scores by
+about one unit, more than the typical gap between the two best base logits.  The GRU
+state, E, G and F are the real ones (1024, and the larger target's 1536);
+only the vocabulary is cut to 20,000 rows (several LM-head tiles and a
+ragged tail) so that the fp64 oracle stays fast.  Every case checks that the
+oracle's values are far above the tolerance, so no comparison can pass
+vacuously (page "Add correctness-first Domino support to DFlash V2",
+sections "Design" (GRU seeding and feedback) and "Validation" (full-chain
+and batch-independence suites)).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_draft_lm_gb300 import inputs
+
+from helpers import (TOL, cached_oracle_weights, cached_weights, check_against_oracle, check_free_run,
+                     device_requests, device_weights, gpu_debug, make_engine)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+V_REDUCED = 20000
+Q8 = inputs.Shape(V=V_REDUCED, H=4096, E=1024, G=1024, F=1024, dtype="bf16")
+QL = inputs.Shape(V=V_REDUCED, H=5120, E=1536, G=1536, F=1536, dtype="bf16")
+
+
+def feedback_scales(sh):
+    return (("emb", 1.0), ("w_ih", sh.E ** -0.5), ("w_hh", sh.G ** -0.5), ("fc1", sh.G ** -0.5),
+            ("fc2", sh.F ** -0.5))
+
+
+def _setup(sh, B, seed0):
+    sc = feedback_scales(sh)
+    w = cached_weights(sh, 0, sc)
+    ow = cached_oracle_weights(sh, 0, sc)
+    r = inputs.make_requests(sh, list(range(seed0, seed0 + B)))
+    return sc, w, ow, r
+
+
+def _not_vacuous(o, r, tol):
+    """The compared quantities must be far larger than the tolerance."""
+    assert np.abs(o["h"]).max() > 20 * tol, np.abs(o["h"]).max()
+    fc1h = o["z"] - oracle.widen(r["s"])[:, 1:15]  # the GRU-dependent part of z
+    assert np.abs(fc1h).max() > 10 * tol, np.abs(fc1h).max()
+
+
+# (shape, B, K): the persistent driver (B = 1), the CUDA-core batched GRU and
+# projector (2 <= B < 12) with the tensor-core correction (K0), the gathered
+# pool correction (B = 3) or the masked dense one (B = 8), and the tensor-core
+# GRU and projector (B >= 12)
+CASES = [(Q8, 1, 0), (Q8, 1, 2048), (Q8, 3, 2048), (Q8, 8, 0), (Q8, 8, 2048), (Q8, 16, 0), (Q8, 64, 0),
+         (Q8, 64, 2048), (QL, 1, 0), (QL, 8, 0), (QL, 64, 0), (QL, 64, 2048)]
+
+
+@pytest.mark.parametrize("sh,B,K", CASES, ids=[f"{'q8' if c[0] is Q8 else 'large'}-B{c[1]}-K{c[2]}" for c in CASES])
+def test_full_hidden_sizes_with_feedback(sh, B, K):
+    sc, w, ow, r = _setup(sh, B, 300)
+    o = oracle.rollout(ow, r["hidden"], r["s"], r["verified"], K)
+    tol = TOL[sh.dtype]
+    _not_vacuous(o, r, tol)
+    eng = make_engine(sh, max_B=B, max_K=K, dw=device_weights(w))
+    dreq = device_requests(r)
+    g = gpu_debug(eng, sh, dreq, B, K, o["tokens"])
+    check_against_oracle(ow, o, g, sh, K)
+    free = eng.run(*dreq, K=K)
+    torch.cuda.synchronize()
+    assert eng.status() == 0
+    check_free_run(o, free.cpu().numpy(), tol)
+    eng.close()
+
+
+@pytest.mark.parametrize("sh,B,K", [(Q8, 1, 0), (Q8, 8, 0), (Q8, 64, 2048), (QL, 64, 0)],
+                         ids=["q8-B1-K0", "q8-B8-K0", "q8-B64-K2048", "large-B64-K0"])
+def test_feedback_changes_tokens(sh, B, K):
+    """Feeding the GRU another chain changes later proposals, in the oracle and
+    identically on the GPU: the feedback path decides tokens here."""
+    sc, w, ow, r = _setup(sh, B, 400)
+    free = oracle.rollout(ow, r["hidden"], r["s"], r["verified"], K)
+    rng = np.random.default_rng(7)
+    other = free["tokens"].copy()
+    other[:, 1:] = rng.integers(0, sh.V, size=(B, 14))  # keep p_1, replace the fed proposals
+    o = oracle.rollout(ow, r["hidden"], r["s"], r["verified"], K, forced=other)
+    changed = (o["tokens"][:, 2:] != free["tokens"][:, 2:]).mean()
+    assert changed > 0.2, f"only {changed:.0%} of the later proposals depend on the fed chain"
+    eng = make_engine(sh, max_B=B, max_K=K, dw=device_weights(w))
+    g = gpu_debug(eng, sh, device_requests(r), B, K, other)
+    check_against_oracle(ow, o, g, sh, K)
+    eng.close()
+
+
+@pytest.mark.parametrize("B,K", [(1, 0), (3, 2048)])
+def test_persistent_and_per_phase_states_agree_tightly(B, K):
+    """The persistent driver's merged GRU update (each CTA rebuilds the state
+    from hidden-side products other CTAs wrote) against the per-phase kernels,
+    teacher-forced on one chain: both keep the state in fp32, so they agree far
+    inside the bf16 tolerance at every one of the 15 updates."""
+    from speculative_decoding_draft_lm_gb300 import rollout as R
+    sc, w, ow, r = _setup(Q8, B, 500)
+    o = oracle.rollout(ow, r["hidden"], r["s"], r["verified"], K)
+    eng = make_engine(Q8, max_B=B, max_K=K, dw=device_weights(w))
+    dreq = device_requests(r)
+    got = {}
+    for drv in (R.DOMINO_DRIVER_KERNELS, R.DOMINO_DRIVER_PERSISTENT):
+        eng.set_driver(drv)
+        got[drv] = gpu_debug(eng, Q8, dreq, B, K, o["tokens"])
+        check_against_oracle(ow, o, got[drv], Q8, K)
+    hk, hp = got[R.DOMINO_DRIVER_KERNELS]["h"], got[R.DOMINO_DRIVER_PERSISTENT]["h"]
+    zk, zp = got[R.DOMINO_DRIVER_KERNELS]["z"], got[R.DOMINO_DRIVER_PERSISTENT]["z"]
+    assert np.abs(hk).max() > 0.2
+    np.testing.assert_allclose(hp, hk, rtol=0, atol=1e-4)
+    np.testing.assert_allclose(zp, zk, rtol=0, atol=1e-4)
+    eng.close()
