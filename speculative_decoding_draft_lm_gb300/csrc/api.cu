@@ -384,6 +384,12 @@ int domino_rollout_set_proposals(domino_ctx* c, int n) {
     return DOMINO_OK;
 }
 
+int domino_rollout_debug_drop_barrier_arrival(domino_ctx* c, int n) {
+    if (!c || n < 0) return DOMINO_ERR_INVALID_ARG;
+    c->drop_barrier = n;
+    return DOMINO_OK;
+}
+
 int domino_rollout_status(domino_ctx* c, void* stream) {
     if (!c) return DOMINO_ERR_INVALID_ARG;
     DeviceGuard guard(c->device);

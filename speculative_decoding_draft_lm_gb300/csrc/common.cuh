@@ -160,6 +160,7 @@ struct domino_ctx {
     int n_proposals;  // early stop: proposals per block (1..15)
     int partitions;   // vocabulary shards of the compact pool construction (1 = direct)
     int last_launches;
+    int drop_barrier;  // test hook of the timeout path (0 = off): see domino_rollout_debug_drop_barrier_arrival
     bool loaded;
     // borrowed weights
     const void *lm_head, *emb, *w_ih, *w_hh, *fc1, *fc2, *bias;

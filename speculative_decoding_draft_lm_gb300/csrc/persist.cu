@@ -69,6 +69,7 @@ struct PersistParams {
     int n_slots;
     int n_cons;     // consumer warps of the correction phase (divides n_slots)
     int slot_bytes;
+    int drop_barrier;  // test hook: CTA 0 skips its arrival at this grid barrier (0 = never)
 };
 
 __device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
@@ -80,12 +81,14 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 }
 
 // Grid barrier among the consumer warps of every CTA.  `n` counts barriers
-// passed so far; the counter was zeroed before the launch.
-__device__ bool grid_sync(unsigned* counter, unsigned& n, volatile int* abort_flag, int* err) {
+// passed so far; the counter was zeroed before the launch.  drop_at == n
+// (a test hook for the timeout path) withholds this CTA's arrival, so every
+// CTA's bounded wait at that barrier runs out.
+__device__ bool grid_sync(unsigned* counter, unsigned& n, volatile int* abort_flag, int* err, int drop_at) {
     cons_sync();
     ++n;
     if (threadIdx.x == 0) {
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+        if (drop_at != (int)n) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
         const unsigned target = n * gridDim.x;
         const unsigned long long t0 = tc::globaltimer();
         while (ld_acquire(counter) < target) {
@@ -348,6 +351,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     if (!full_vocab) pdl_wait();
     unsigned nsync = 0;
     unsigned* counter = p.sync;
+    const int drop_at = blockIdx.x == 0 ? p.drop_barrier : 0;
     // static per-CTA bias values of the slice
     for (int i = tid; i < nw; i += kConsumerWarps * 32) {
         const int v = full_vocab ? (int)(w0 + i) : p.pool[w0 + i];
@@ -708,22 +712,22 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
         gru(0, false);  // the verified token: independent of the previous kernel
         stamp();                                                     // 1
         pdl_wait();     // base logits, p_1 and the cleared argmax words are ready
-        if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+        if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
         stamp();                                                     // 2
         gru(1, false);
         stamp();                                                     // 3
-        if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+        if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
         stamp();                                                     // 4
         for (int k = 1; k <= p.n_corr; ++k) {                        // 5 + 6 (k-1) + ...
             prefetch_L(k);
             // one request group: GRU update k joins the projector phase
             fc1(k, pre_gh && k > 1);
             stamp();                                                 // +0 projector done
-            if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+            if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
             stamp();                                                 // +1 barrier
             correct(k);
             stamp();                                                 // +2 correction done
-            if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+            if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
             stamp();                                                 // +3 barrier
             if (k < p.n_corr) {
                 if (pre_gh) {  // the next update runs in the next projector phase
@@ -732,7 +736,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                 } else {
                     gru(k + 1, false);
                     stamp();                                         // +4 GRU done
-                    if (!grid_sync(counter, nsync, abort_flag, p.err)) return;
+                    if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
                     stamp();                                         // +5 barrier
                 }
             }
@@ -843,6 +847,8 @@ cudaError_t launch_t(domino_ctx* c, RunArgs& r) {
     p.n_slots = n_slots;
     p.n_cons = n_cons;
     p.slot_bytes = slot_bytes;
+    p.drop_barrier = c->drop_barrier;  // one-shot test hook
+    c->drop_barrier = 0;
 
     const int mx = g.E > g.G ? (g.E > g.F ? g.E : g.F) : (g.G > g.F ? g.G : g.F);
     const int nch = (mx + 255) / 256;

@@ -39,6 +39,7 @@ EXPORTED = (
     "domino_rollout_last_launch_count", "domino_rollout_destroy", "domino_rollout_strerror",
     "domino_rollout_enable_timing", "domino_rollout_read_timing", "domino_candidate_pool_static",
     "domino_rollout_set_proposals", "domino_rollout_load_backbone_proj", "domino_rollout_set_vocab_partitions",
+    "domino_rollout_debug_drop_barrier_arrival",
 )
 
 PHASES = ("lmhead", "argmax", "pool", "gru", "fc1", "correct", "steps", "other")
@@ -93,6 +94,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.domino_rollout_set_proposals.argtypes = [vp, i]
     lib.domino_rollout_load_backbone_proj.argtypes = [vp, vp]
     lib.domino_rollout_set_vocab_partitions.argtypes = [vp, i]
+    lib.domino_rollout_debug_drop_barrier_arrival.argtypes = [vp, i]
     lib.domino_rollout_strerror.argtypes = [i]
     lib.domino_rollout_strerror.restype = ctypes.c_char_p
     for name in EXPORTED:
@@ -167,6 +169,11 @@ def domino_rollout_set_vocab_partitions(ctx, P: int) -> int:
 
 def domino_rollout_set_proposals(ctx, n: int) -> int:
     return _check(load_library().domino_rollout_set_proposals(ctx, n), "domino_rollout_set_proposals")
+
+
+def domino_rollout_debug_drop_barrier_arrival(ctx, n: int) -> int:
+    """Test hook of the timeout path (see the header): returns the status."""
+    return load_library().domino_rollout_debug_drop_barrier_arrival(ctx, n)
 
 
 def domino_rollout_status(ctx, stream=None) -> int:

@@ -51,6 +51,7 @@ def test_strerror_and_null_handles(lib):
     assert lib.domino_rollout_load_backbone_proj(None, None) == R.DOMINO_ERR_INVALID_ARG
     assert lib.domino_rollout_enable_timing(None, 1) == R.DOMINO_ERR_INVALID_ARG
     assert lib.domino_candidate_pool_static(None, 1, 10, 2, None, None) == R.DOMINO_ERR_INVALID_ARG
+    assert lib.domino_rollout_debug_drop_barrier_arrival(None, 1) == R.DOMINO_ERR_INVALID_ARG
     lib.domino_rollout_destroy(None)
     assert lib.domino_rollout_last_launch_count(None) == 0
 
