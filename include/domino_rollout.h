@@ -211,6 +211,20 @@ DOMINO_API int domino_rollout_set_vocab_partitions(domino_ctx* ctx, int P);
  * if the stream reported an error. */
 DOMINO_API int domino_rollout_status(domino_ctx* ctx, void* cuda_stream);
 
+/* Test hook of the device-side timeout path (page "Add correctness-first
+ * Domino support to DFlash V2", section "Supported and numerical scope":
+ * clear errors, no silent fallback).  Off by default and one-shot: with
+ * n >= 1, the next run that uses the persistent driver makes its first CTA
+ * withhold its arrival at the driver's n-th grid barrier (barriers 1 and 2
+ * follow the two seed updates; each corrected step then has two, or three
+ * for more than four requests).  No other arrival replaces it, so the
+ * bounded wait of every CTA at that barrier runs out after 200 ms, the
+ * kernel returns, the run's tokens are meaningless and
+ * domino_rollout_status() reports DOMINO_ERR_TIMEOUT.  Nothing faults or
+ * hangs and the context stays usable; that run clears the hook (n = 0 clears
+ * it by hand).  Errors: INVALID_ARG (null ctx, n < 0). */
+DOMINO_API int domino_rollout_debug_drop_barrier_arrival(domino_ctx* ctx, int n);
+
 /* Number of kernel launches the last run()/debug_run() enqueued. */
 DOMINO_API int domino_rollout_last_launch_count(const domino_ctx* ctx);
 
@@ -230,7 +244,9 @@ DOMINO_API int domino_rollout_last_launch_count(const domino_ctx* ctx);
  * [B,K] int32 (DEVICE, caller-owned) on `cuda_stream`, for the current device.
  *
  * The first call on a device looks up the buffer's device address on that
- * device; make that first call before any stream capture.  All calls share
+ * device and keeps it for the life of the process; make that first call
+ * before any stream capture.  A cudaDeviceReset() of that device afterwards
+ * invalidates the kept address: do not call this entry point after one.  All calls share
  * the one buffer and every call overwrites it, so calls whose kernels can
  * overlap on the GPU (different streams without ordering) race and must be
  * serialised by the caller.  Requires 0 < K < V and V <= 431000.  Errors:
