@@ -156,10 +156,18 @@ DOMINO_API int domino_rollout_debug_run(domino_ctx* ctx, const void* hidden, con
                              const int32_t* forced_tokens, const domino_debug_bufs* dbg,
                              int32_t* out_tokens, void* cuda_stream);
 
-/* Driver of the 14 dependent steps. */
-#define DOMINO_DRIVER_AUTO       0  /* pick per (B, K)                              */
-#define DOMINO_DRIVER_KERNELS    1  /* one launch per phase, stream-ordered         */
-#define DOMINO_DRIVER_PERSISTENT 2  /* one cooperative launch with grid barriers    */
+/* Driver of the 14 dependent steps.  The persistent drivers are one
+ * cooperative launch (one CTA per SM).  The tagged-exchange one covers bf16,
+ * B <= 4 (B = 1 for the full vocabulary), G, F <= 1024 and V < 2^18: its CTAs
+ * pass activations, hidden-side products and per-CTA bests through words
+ * that carry the step they belong to, instead of meeting at grid barriers.
+ * DOMINO_DRIVER_PERSISTENT takes it where it applies and the grid-barrier
+ * kernel elsewhere; DOMINO_DRIVER_PERSISTENT_GRID always the latter.  A
+ * persistent driver that does not cover the run gives UNSUPPORTED. */
+#define DOMINO_DRIVER_AUTO            0  /* pick per (B, K)                              */
+#define DOMINO_DRIVER_KERNELS         1  /* one launch per phase, stream-ordered         */
+#define DOMINO_DRIVER_PERSISTENT      2  /* one cooperative launch (see above)           */
+#define DOMINO_DRIVER_PERSISTENT_GRID 3  /* one cooperative launch with grid barriers    */
 DOMINO_API int domino_rollout_set_driver(domino_ctx* ctx, int driver);
 
 /* Per-phase timing.  When enabled, run()/debug_run() record a pair of CUDA
@@ -214,12 +222,15 @@ DOMINO_API int domino_rollout_status(domino_ctx* ctx, void* cuda_stream);
 /* Test hook of the device-side timeout path (page "Add correctness-first
  * Domino support to DFlash V2", section "Supported and numerical scope":
  * clear errors, no silent fallback).  Off by default and one-shot: with
- * n >= 1, the next run that uses the persistent driver makes its first CTA
- * withhold its arrival at the driver's n-th grid barrier (barriers 1 and 2
- * follow the two seed updates; each corrected step then has two, or three
- * for more than four requests).  No other arrival replaces it, so the
- * bounded wait of every CTA at that barrier runs out after 200 ms, the
- * kernel returns, the run's tokens are meaningless and
+ * n >= 1, the next run that uses a persistent driver makes its first CTA
+ * withhold its n-th synchronisation: its arrival at the n-th grid barrier
+ * (barriers 1 and 2 follow the two seed updates; each corrected step then
+ * has two, or three for more than four requests), or in the tagged-exchange
+ * driver its n-th publication (1: the seed's hidden-side products; then per
+ * step its activations, its hidden-side products of the next update unless
+ * the step is the last, and its best).  Nothing replaces it, so the bounded
+ * wait of every CTA for it runs out after 200 ms, the kernel returns, the
+ * run's tokens are meaningless and
  * domino_rollout_status() reports DOMINO_ERR_TIMEOUT.  Nothing faults or
  * hangs and the context stays usable; that run clears the hook (n = 0 clears
  * it by hand).  Errors: INVALID_ARG (null ctx, n < 0). */

@@ -87,14 +87,18 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     r.out_tokens = out;
     r.st = (cudaStream_t)stream;
 
-    bool use_persist = false;
+    // 0: per-phase kernels, 1: grid-barrier persistent kernel, 2: tagged-exchange persistent kernel
+    int persist_kind = 0;
     if (c->driver == DOMINO_DRIVER_PERSISTENT) {
-        if (!persist_supported(c, r)) return DOMINO_ERR_UNSUPPORTED;
-        use_persist = true;
+        persist_kind = persist_ll_supported(c, r) ? 2 : persist_supported(c, r) ? 1 : -1;
+    } else if (c->driver == DOMINO_DRIVER_PERSISTENT_GRID) {
+        persist_kind = persist_supported(c, r) ? 1 : -1;
     } else if (c->driver == DOMINO_DRIVER_AUTO) {
-        // one request: the persistent driver; batches: the batched kernels
-        use_persist = r.B == 1 && persist_supported(c, r);
+        // one request: a persistent driver; batches: the batched kernels
+        if (r.B == 1) persist_kind = persist_ll_supported(c, r) ? 2 : persist_supported(c, r) ? 1 : 0;
     }
+    if (persist_kind < 0) return DOMINO_ERR_UNSUPPORTED;
+    const bool use_persist = persist_kind > 0;
 
     cudaError_t e;
 #define STEP(phase, x)                                   \
@@ -125,7 +129,7 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         }
     }
     if (use_persist) {
-        STEP(DOMINO_PHASE_STEPS, launch_persist(c, r));
+        STEP(DOMINO_PHASE_STEPS, persist_kind == 2 ? launch_persist_ll(c, r) : launch_persist(c, r));
     } else {
     const bool batch = r.B >= 2 && batch_kernels_supported(c);
     // bf16 batches: GRU and projector layer 1 as tensor-core contractions
@@ -223,10 +227,14 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oWp = take(gru_tc ? (size_t)4 * gru_padded_units(g.G) * g.G * 2 : 0);
     size_t oX = take(gru_tc ? (size_t)2 * c->a_rows * g.G * 2 : 0);
     size_t oT = take((size_t)g.V * 3 * g.G * sizeof(float));
-    size_t oGh = take((size_t)4 * 3 * g.G * sizeof(float));
+    size_t oGh = take((size_t)kPersistGruGroup * 3 * g.G * sizeof(float));
     const bool pmask = g.max_K > 0 && g.dtype == DOMINO_DTYPE_BF16;
     size_t oM = take(pmask ? (size_t)g.max_B * pool_mask_words(g.V) * 4 : 0);
     size_t oC = take(g.max_K > 0 ? (size_t)g.max_B * DOMINO_MAX_VOCAB_PARTITIONS * g.max_K * 4 : 0);
+    const bool ll = g.dtype == DOMINO_DTYPE_BF16;  // tagged-exchange persistent driver
+    size_t oXa = take(ll ? (size_t)2 * kLLMaxBatch * g.F * 8 : 0);
+    size_t oXg = take(ll ? (size_t)2 * kLLMaxBatch * 3 * g.G * 8 : 0);
+    size_t oXb = take(ll ? (size_t)2 * c->num_sms * kLLMaxBatch * 8 : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -251,6 +259,9 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->gh_next = (float*)(base + oGh);
     c->pmask = pmask ? (uint32_t*)(base + oM) : nullptr;
     c->cand = g.max_K > 0 ? (int32_t*)(base + oC) : nullptr;
+    c->xa = ll ? (unsigned long long*)(base + oXa) : nullptr;
+    c->xgh = ll ? (unsigned long long*)(base + oXg) : nullptr;
+    c->xbest = ll ? (unsigned long long*)(base + oXb) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -340,7 +351,8 @@ int domino_rollout_debug_run(domino_ctx* c, const void* hidden, const void* s, c
 
 int domino_rollout_set_driver(domino_ctx* c, int driver) {
     if (!c) return DOMINO_ERR_INVALID_ARG;
-    if (driver != DOMINO_DRIVER_AUTO && driver != DOMINO_DRIVER_KERNELS && driver != DOMINO_DRIVER_PERSISTENT)
+    if (driver != DOMINO_DRIVER_AUTO && driver != DOMINO_DRIVER_KERNELS && driver != DOMINO_DRIVER_PERSISTENT &&
+        driver != DOMINO_DRIVER_PERSISTENT_GRID)
         return DOMINO_ERR_INVALID_ARG;
     c->driver = driver;
     return DOMINO_OK;

@@ -179,9 +179,12 @@ struct domino_ctx {
     unsigned long long* keys; // [max_B,16] argmax words, one per proposal
     int* bad;                 // [max_B] request saw an invalid token
     int* err;                 // device error word
-    unsigned int* sync;       // grid-barrier words for the persistent driver
+    unsigned int* sync;       // grid-barrier words, per-step claim counters and the run counter
+    unsigned long long* xa;     // [2][kLLMaxBatch,F] tagged activations (tagged-exchange driver)
+    unsigned long long* xgh;    // [2][kLLMaxBatch,3G] tagged hidden-side products
+    unsigned long long* xbest;  // [2][num_sms,kLLMaxBatch] per-CTA best of a step
     float* gi_table;          // [V, 3G] input-side GRU pre-activations of every token (built at load)
-    float* gh_next;           // [4][3G] hidden-side pre-activations of the next GRU update (persistent driver)
+    float* gh_next;           // [kPersistGruGroup][3G] hidden-side pre-activations of the next GRU update (persistent driver)
     __nv_bfloat16* wp;        // [4*Gp, G] packed hidden-side GRU weights (bf16 batches), or null
     __nv_bfloat16* h16;       // [2][a_rows, G] bf16 copies of the GRU state (tensor-core operands)
     void* ws_base;            // single workspace allocation

@@ -106,9 +106,19 @@ cudaError_t prepare_gru_tc(domino_ctx* c, RunArgs& r, GruMaps* m);
 cudaError_t launch_gru_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int u);
 cudaError_t launch_fc1_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int k);
 
-// persistent driver of the GRU seed and the 14 corrected steps (persist.cu)
+// persistent driver of the GRU seed and the 14 corrected steps (persist.cu).
+// Requests per GRU/projector staging group; the workspace's hidden-side
+// products of the next update (domino_ctx::gh_next) hold one group.
+constexpr int kPersistGruGroup = 4;
 bool persist_supported(const domino_ctx* c, const RunArgs& r);
 cudaError_t launch_persist(domino_ctx* c, RunArgs& r);
+
+// persistent driver with tagged data exchanges for small batches (persist_ll.cu)
+constexpr int kLLMaxBatch = 4;        // requests it covers
+constexpr int kClaimCounters = 16;    // sync words 16..31: per-step shared-chunk counters (cleared per run)
+constexpr int kRunEpochWord = 64;     // sync word 64: run counter (bumped per run, never cleared)
+bool persist_ll_supported(const domino_ctx* c, const RunArgs& r);
+cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r);
 
 // index of the ping-pong h buffer written by GRU update u
 __host__ __device__ inline int h_slot(int u) { return u & 1; }

@@ -20,13 +20,15 @@ inline int grid_for(int items_per_block_unit, int units, int cap) {
 
 // ---------------------------------------------------------------------------
 __global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__ bad, unsigned* __restrict__ sync,
-                        int n_keys, int B) {
+                        unsigned long long* __restrict__ xbest, int n_keys, int B, int n_xbest) {
     pdl_trigger();
     pdl_wait();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n_keys) keys[i] = 0ull;
     if (i < B) bad[i] = 0;
     if (i < 64) sync[i] = 0u;  // grid-barrier counter and the per-step chunk counters
+    if (i < n_xbest) xbest[i] = 0ull;  // per-CTA bests of the tagged-exchange driver
+    if (i == 0) sync[kRunEpochWord] += 1u;  // a new tag range for this run's exchange words
 }
 
 // ---------------------------------------------------------------------------
@@ -430,9 +432,12 @@ __global__ void __launch_bounds__(256) k_backbone_s(const T* __restrict__ hidden
     } while (0)
 
 cudaError_t launch_reset(domino_ctx* c, RunArgs& r) {
-    int n = r.B * kBlock;
+    const int n = r.B * kBlock;
+    const int nx = c->xbest ? 2 * c->num_sms * kLLMaxBatch : 0;
+    const int m = n > nx ? n : nx;
     ++r.launches;
-    return launch_pdl(k_reset, dim3((n + 255) / 256), dim3(256), 0, r.st, c->keys, c->bad, c->sync, n, r.B);
+    return launch_pdl(k_reset, dim3((m + 255) / 256), dim3(256), 0, r.st, c->keys, c->bad, c->sync, c->xbest, n, r.B,
+                      nx);
 }
 
 cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r) {

@@ -31,22 +31,23 @@
 // or pool entries of any request.  Every wait (grid barrier, ring slot) is
 // bounded; on a timeout the kernel raises the device error word and returns.
 #include "internal.h"
+#include "persist_util.cuh"
 #include "tc_common.cuh"
 
 namespace domino {
 
 namespace {
 
+using namespace persist;
 // 15 consumer warps + 1 producer warp: 16 warps leave 128 registers a thread
-constexpr int kConsumerWarps = 15;
-constexpr int kPersistThreads = (kConsumerWarps + 1) * 32;
+constexpr int kPersistThreads = persist::kThreads;
 constexpr int kRowsPerSlot = 4;    // rows per ring slot; one warp consumes a whole slot
 constexpr int kMaxSlots = 48;
 // Ring slot q % n_slots is consumed by warp q % n_cons alone (n_cons divides
 // n_slots): each slot has one waiting consumer and the producer, so a parity
 // wait can never observe a fill that belongs to a later pass over the ring.
 constexpr int kMaxReq = 8;         // requests a CTA may touch in phase C
-constexpr int kGruGroup = 4;       // requests per GRU/fc1 staging group
+constexpr int kGruGroup = kPersistGruGroup;  // requests per GRU/fc1 staging group
 constexpr int kMaxSeg = 2048;      // rows (or pool entries) per CTA
 
 template <typename T>
@@ -72,14 +73,6 @@ struct PersistParams {
     int drop_barrier;  // test hook: CTA 0 skips its arrival at this grid barrier (0 = never)
 };
 
-__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Grid barrier among the consumer warps of every CTA.  `n` counts barriers
 // passed so far; the counter was zeroed before the launch.  drop_at == n
 // (a test hook for the timeout path) withholds this CTA's arrival, so every
@@ -104,117 +97,6 @@ __device__ bool grid_sync(unsigned* counter, unsigned& n, volatile int* abort_fl
     return !*abort_flag;
 }
 
-__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// 8 consecutive elements of a shared-memory row widened to fp32
-__device__ __forceinline__ void lds8(const float* p, float* o) {
-    float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
-    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
-}
-__device__ __forceinline__ void lds8(const __nv_bfloat16* p, float* o) {
-    uint4 q = *reinterpret_cast<const uint4*>(p);
-    bf16x2_to_f32(q.x, o[0], o[1]);
-    bf16x2_to_f32(q.y, o[2], o[3]);
-    bf16x2_to_f32(q.z, o[4], o[5]);
-    bf16x2_to_f32(q.w, o[6], o[7]);
-}
-
-// One weight row held in registers: lane l owns elements (l + 32 c) * 8 .. +7
-// for c < NCH (NCH * 256 >= row length).  All chunks are requested before any
-// is used, with an L2 evict-last hint (these small matrices are re-read every
-// step while fc2 streams past them).
-template <typename T, int NCH>
-struct RegRow;
-template <int NCH>
-struct RegRow<__nv_bfloat16, NCH> {
-    uint4 q[NCH];
-    __device__ __forceinline__ void load(const __nv_bfloat16* row, int n, int lane, uint64_t pol) {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int e = (lane + 32 * c) * 8;
-            if (e < n)
-                asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                             : "=r"(q[c].x), "=r"(q[c].y), "=r"(q[c].z), "=r"(q[c].w)
-                             : "l"(row + e), "l"(pol));
-            else
-                q[c] = make_uint4(0, 0, 0, 0);
-        }
-    }
-    __device__ __forceinline__ void get(int c, float* o) const {
-        bf16x2_to_f32(q[c].x, o[0], o[1]);
-        bf16x2_to_f32(q[c].y, o[2], o[3]);
-        bf16x2_to_f32(q[c].z, o[4], o[5]);
-        bf16x2_to_f32(q[c].w, o[6], o[7]);
-    }
-};
-template <int NCH>
-struct RegRow<float, NCH> {
-    float4 q[2 * NCH];
-    __device__ __forceinline__ void load(const float* row, int n, int lane, uint64_t pol) {
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int e = (lane + 32 * c) * 8;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (e < n)
-                    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-                                 : "=f"(q[2 * c + h].x), "=f"(q[2 * c + h].y), "=f"(q[2 * c + h].z),
-                                   "=f"(q[2 * c + h].w)
-                                 : "l"(row + e + 4 * h), "l"(pol));
-                else
-                    q[2 * c + h] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-    }
-    __device__ __forceinline__ void get(int c, float* o) const {
-        o[0] = q[2 * c].x; o[1] = q[2 * c].y; o[2] = q[2 * c].z; o[3] = q[2 * c].w;
-        o[4] = q[2 * c + 1].x; o[5] = q[2 * c + 1].y; o[6] = q[2 * c + 1].z; o[7] = q[2 * c + 1].w;
-    }
-};
-
-// dot of a register row with a shared-memory fp32 vector (same element map)
-template <typename T, int NCH>
-__device__ __forceinline__ float row_dot_smem(const RegRow<T, NCH>& w, const float* x, int n, int lane) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int e = (lane + 32 * c) * 8;
-        if (e < n) {
-            float ww[8], xx[8];
-            w.get(c, ww);
-            lds8(x + e, xx);
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                a0 = fmaf(ww[i], xx[i], a0);
-                a1 = fmaf(ww[i + 1], xx[i + 1], a1);
-            }
-        }
-    }
-    return a0 + a1;
-}
-
-// Sum each of 4 per-lane values over the warp with 6 shuffles (a transposed
-// butterfly).  Lane l ends with the total of value ((l >> 4) & 1) * 2 +
-// ((l >> 3) & 1).
-__device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v3, int lane) {
-    const bool hi16 = (lane & 16) != 0;
-    float a = hi16 ? v2 : v0, b = hi16 ? v3 : v1;          // keep
-    float c = hi16 ? v0 : v2, d = hi16 ? v1 : v3;          // send
-    a += __shfl_xor_sync(0xffffffffu, c, 16);
-    b += __shfl_xor_sync(0xffffffffu, d, 16);
-    const bool hi8 = (lane & 8) != 0;
-    float keep = hi8 ? b : a, send = hi8 ? a : b;
-    keep += __shfl_xor_sync(0xffffffffu, send, 8);
-    keep += __shfl_xor_sync(0xffffffffu, keep, 4);
-    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-    keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-    return keep;
-}
-
 // Shared-memory layout (bytes, all offsets 128-aligned)
 // Requests whose activations one CTA needs in phase C.
 __host__ __device__ inline int phase_c_requests(int B, int K, int seg) {
@@ -233,7 +115,7 @@ struct Layout {
         bars = o; o = up(o + 16 * n_slots);
         sa = o;   o = up(o + 4 * nreq * F);
         sh = o;   o = up(o + 4 * ngru * G);
-        sg = o;   o = up(o + 4 * 9 * kGruGroup * 64);   // gate products + next hidden-side products
+        sg = o;   o = up(o + 4 * 3 * kGruGroup * 64);   // hidden-side products of one request group
         sL = o;   o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
         stot = o; o = up(o + 4 * seg);
@@ -369,10 +251,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     // (its warps have slack while fc2 streams) when all requests fit one group
     const bool pre_gh = B <= kGruGroup;
 
-    // ---- one GRU update u for every request; writes h[slot(u)].  With
-    // gh_ready, the hidden-side products are in p.gh and h_in is still staged
-    // in sh (it was staged for the projector of the same step).
-    auto gru = [&](int u, bool gh_ready) {
+    // ---- one GRU update u for every request; writes h[slot(u)]
+    auto gru = [&](int u) {
         const float* h_in = p.h + (size_t)h_slot(u + 1) * p.max_B * G;
         float* h_out = p.h + (size_t)h_slot(u) * p.max_B * G;
         if (tid < B) {
@@ -389,7 +269,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
             }
             stok[tid] = t;
         }
-        const bool need_gh = u > 0 && !gh_ready;
+        const bool need_gh = u > 0;
         for (int g0 = 0; g0 < B; g0 += kGruGroup) {
             const int ng = min(kGruGroup, B - g0);
             // the input side W_ih x of every request is a row of the token table;
@@ -414,7 +294,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                     for (int b = 0; b < kGruGroup; ++b) {
                         if (b < ng) {
                             const float gh = warp_sum(row_dot_smem(wh, sh + b * G, G, lane));
-                            if (lane == 0) sg[((jj * 3 + gate) * kGruGroup + b) * 2 + 1] = gh;
+                            if (lane == 0) sg[(jj * 3 + gate) * kGruGroup + b] = gh;
                         }
                     }
                 }
@@ -425,9 +305,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                 const float* gi = p.gi_table + (size_t)stok[g0 + b] * 3 * G + j0 + jj;
                 float gh[3];
 #pragma unroll
-                for (int q = 0; q < 3; ++q)
-                    gh[q] = need_gh ? sg[((jj * 3 + q) * kGruGroup + b) * 2 + 1]
-                                    : (u > 0 ? p.gh[((size_t)(g0 + b) * 3 + q) * G + j0 + jj] : 0.f);
+                for (int q = 0; q < 3; ++q) gh[q] = need_gh ? sg[(jj * 3 + q) * kGruGroup + b] : 0.f;
                 const float r = sigmoidf_(__ldg(gi) + gh[0]);
                 const float zg = sigmoidf_(__ldg(gi + G) + gh[1]);
                 const float n = tanhf(__ldg(gi + 2 * G) + r * gh[2]);
@@ -709,12 +587,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
     };
     auto body = [&]() {
         stamp();                                                     // 0: start
-        gru(0, false);  // the verified token: independent of the previous kernel
+        gru(0);  // the verified token: independent of the previous kernel
         stamp();                                                     // 1
         pdl_wait();     // base logits, p_1 and the cleared argmax words are ready
         if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
         stamp();                                                     // 2
-        gru(1, false);
+        gru(1);
         stamp();                                                     // 3
         if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
         stamp();                                                     // 4
@@ -734,7 +612,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_rollout_persist(PersistP
                     stamp();                                         // +4
                     stamp();                                         // +5
                 } else {
-                    gru(k + 1, false);
+                    gru(k + 1);
                     stamp();                                         // +4 GRU done
                     if (!grid_sync(counter, nsync, abort_flag, p.err, drop_at)) return;
                     stamp();                                         // +5 barrier

@@ -1,0 +1,901 @@
+// Persistent driver for small batches (B <= 4, bf16) whose CTAs exchange
+// data through step-tagged words instead of meeting at grid barriers.
+//
+// Per corrected step k (page "Add correctness-first Domino support to DFlash
+// V2", section "Design"; page "[Spec] Add Domino projector support to DFlash
+// speculative decoding (V2)", section "Implementation"):
+//   P_k  every CTA holds the whole state h_k in shared memory; it computes its
+//        slice of a = SiLU(fc1 h_k + s[k]) and publishes it, then its units'
+//        hidden-side products W_hh h_k of the next GRU update, and publishes
+//        them too;
+//   C_k  every CTA reads all of a, scores its slice of fc2 rows (full
+//        vocabulary, B = 1) or of the pool entries,
+//        c[v] = fc2[v].a + bias[v] + L[b,k+1,v], and publishes its best
+//        (value, id) per request;
+//   then every CTA reads all the bests, takes p_{k+1} (lowest id on ties),
+//   and rebuilds h_{k+1} = GRU(emb[p_{k+1}], h_k) for all units from the
+//   token-table row and the published hidden-side products.
+//
+// Exchange words are 64 bits: a 32-bit payload with a 32-bit tag (run epoch
+// * 16 + step), or for the per-CTA bests the packed key (orderable value, low
+// id first) with the step in the low bits.  One 8-byte store publishes value
+// and tag together, and a reader polls the word until its tag is the one it
+// waits for, so a read of the data is also the synchronisation (no separate
+// barrier round trip).  Each word has one writer per step.  Every exchange
+// is double-buffered by step parity: a CTA that publishes nothing another one
+// waits for (e.g. one without projector rows) may still be reading step k's
+// words when a faster CTA publishes step k+1, but no CTA can publish step
+// k+2 before every CTA has published something that follows its reading of
+// step k (its best of step k or k+1), so a buffer is never overwritten while
+// it is read.
+//
+// The W_hh rows of a CTA's units and its fc1 rows stay in shared memory for
+// the whole launch; pool rows too, when they fit.  Over the full vocabulary a
+// producer warp streams fc2 with bulk copies into a ring (walking the slice
+// in alternating directions so a step starts on the rows the last one read);
+// the last seventh of every slice is shared: producers that finish their own
+// part early claim those chunks through a per-step counter, which absorbs the
+// per-step spread of the CTAs' streaming rates.
+//
+// Every wait (exchange word, ring slot) is bounded; on a timeout the kernel
+// raises the device error word, and all consumer warps leave together (the
+// decision is taken with a barrier that ORs their flags).
+#include "internal.h"
+#include "persist_util.cuh"
+
+namespace domino {
+
+using namespace persist;
+
+namespace {
+
+constexpr int kRows = 4;        // fc2 rows per ring slot
+constexpr int kMaxSlots = 64;
+constexpr int kShareDiv = 7;    // a seventh of each full-vocabulary slice is shared
+constexpr int kProducerLanes = 4;  // lanes of the producer warp that issue copies
+constexpr int kMaxSeg = 2048;
+constexpr unsigned kBestTagMask = 0x3FFFu;  // low 14 bits of a best word: the step
+constexpr int kBestIdShift = 14;            // next 18 bits: ~id
+
+struct LLParams {
+    const __nv_bfloat16 *w_hh, *fc1, *fc2, *bias, *s;
+    const float* gi_table;  // [V, 3G]
+    const int32_t *verified, *forced, *pool;
+    const float* L;
+    unsigned long long* keys;
+    int *bad, *err;
+    unsigned* claim;        // [16] per-step shared-chunk counters, zeroed per run
+    const unsigned* epoch;  // run counter, bumped per run before this kernel
+    unsigned long long* xa;     // [2][kLLMaxBatch][F]   by step parity
+    unsigned long long* xgh;    // [2][kLLMaxBatch][3G]  by update parity
+    unsigned long long* xbest;  // [2][grid][kLLMaxBatch] by step parity, zeroed per run
+    float *dbg_h, *dbg_z, *dbg_scores;
+    unsigned long long* trace;
+    int B, K, V, G, F;
+    int n_corr;
+    int seg;        // rows (K0) or pool entries per CTA, a multiple of kRows
+    int jpc, fpc;   // GRU units / fc1 rows per CTA
+    int n_slots, n_cons, resident, pin_gi;
+    int wh_res;     // W_hh rows of the CTA's units kept in shared memory (else read from L2 each step)
+    int drop_at;    // test hook: CTA 0 withholds its publication number drop_at (0 = never)
+};
+
+struct LLLayout {
+    int ring, bars, srow, swhh, sfc1, sh, sa, sL, sbias, stot, spid, ss, sgh0, sred, stok, misc, total;
+    __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B,
+                                 bool wh_res) {
+        auto up = [](int x) { return (x + 127) & ~127; };
+        int o = 0;
+        ring = o;  o = up(o + n_slots * slot_bytes);
+        bars = o;  o = up(o + 16 * n_slots);
+        srow = o;  o = up(o + 4 * n_slots);
+        swhh = o;  o = up(o + (wh_res ? 3 * jpc * G * 2 : 0));
+        sfc1 = o;  o = up(o + fpc * G * 2);
+        sh = o;    o = up(o + 4 * B * G);
+        sa = o;    o = up(o + 4 * B * F);
+        sL = o;    o = up(o + 4 * seg);
+        sbias = o; o = up(o + 4 * seg);
+        stot = o;  o = up(o + 4 * seg);
+        spid = o;  o = up(o + 4 * seg);                        // pool ids of the slice
+        ss = o;    o = up(o + 4 * B * kProposals * fpc);       // s rows of the CTA's projector outputs
+        sgh0 = o;  o = up(o + 4 * B * 3 * jpc);
+        sred = o;  o = up(o + 8 * (kConsumerWarps + 1) * kLLMaxBatch);
+        stok = o;  o = up(o + 4 * kLLMaxBatch);
+        misc = o;  o = up(o + 64);
+        total = o;
+    }
+};
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long tagged(float x, unsigned tag) {
+    return ((unsigned long long)tag << 32) | __float_as_uint(x);
+}
+
+// Spin until the word at p satisfies `ok` (its tag has arrived); bounded.
+// Returns the word; on a timeout (or when another thread of the CTA gave up)
+// sets *failed.
+template <typename Ok>
+__device__ __forceinline__ unsigned long long poll_word(const unsigned long long* p, unsigned long long v, Ok ok,
+                                                        volatile int* abort_flag, int* err, bool& failed) {
+    if (ok(v)) return v;
+    const unsigned long long t0 = tc::globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            v = ld_relaxed_u64(p);
+            if (ok(v)) return v;
+        }
+        if (*abort_flag) {
+            failed = true;
+            return v;
+        }
+        if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeout);
+            failed = true;
+            return v;
+        }
+    }
+}
+
+// dot of a bf16 shared-memory row with an fp32 shared-memory vector, lane
+// partial (lane l covers elements (l + 32c)*8 .. +7)
+template <int NCH>
+__device__ __forceinline__ float smem_dot(const __nv_bfloat16* row, const float* x, int n, int lane) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int e = (lane + 32 * c) * 8;
+        if (e < n) {
+            float w[8], v[8];
+            lds8(row + e, w);
+            lds8(x + e, v);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                a0 = fmaf(w[i], v[i], a0);
+                a1 = fmaf(w[i + 1], v[i + 1], a1);
+            }
+        }
+    }
+    return a0 + a1;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int B = p.B, V = p.V, G = p.G, F = p.F;
+    const size_t row_bytes = (size_t)F * sizeof(__nv_bfloat16);
+    const int slot_bytes = kRows * F * (int)sizeof(__nv_bfloat16);
+    const LLLayout lay(p.n_slots, slot_bytes, G, F, p.jpc, p.fpc, p.seg, B, p.wh_res != 0);
+    uint8_t* ring = sm + lay.ring;
+    const uint32_t full0 = tc::smem_u32(sm + lay.bars), empty0 = full0 + 8 * p.n_slots;
+    volatile int* srow = reinterpret_cast<volatile int*>(sm + lay.srow);
+    const __nv_bfloat16* swhh = reinterpret_cast<const __nv_bfloat16*>(sm + lay.swhh);
+    const __nv_bfloat16* sfc1 = reinterpret_cast<const __nv_bfloat16*>(sm + lay.sfc1);
+    float* sh = reinterpret_cast<float*>(sm + lay.sh);
+    float* sa = reinterpret_cast<float*>(sm + lay.sa);
+    float* sL = reinterpret_cast<float*>(sm + lay.sL);
+    float* sbias = reinterpret_cast<float*>(sm + lay.sbias);
+    float* stot = reinterpret_cast<float*>(sm + lay.stot);
+    int* spid = reinterpret_cast<int*>(sm + lay.spid);
+    float* ss = reinterpret_cast<float*>(sm + lay.ss);
+    float* sgh0 = reinterpret_cast<float*>(sm + lay.sgh0);
+    unsigned long long* sred = reinterpret_cast<unsigned long long*>(sm + lay.sred);
+    int* stok = reinterpret_cast<int*>(sm + lay.stok);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + lay.misc);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const bool full_vocab = p.K == 0;
+    const int grid = gridDim.x, cta = blockIdx.x;
+
+    // this CTA's correction slice: fc2 rows [w0, w1) or pool entries [w0, w1)
+    const long long work = full_vocab ? (long long)V : (long long)B * p.K;
+    const long long w0 = min(work, (long long)cta * p.seg);
+    const long long w1 = min(work, w0 + p.seg);
+    const int nw = (int)(w1 - w0);
+    const int n_chunks = (nw + kRows - 1) / kRows;
+    const int n_share = full_vocab ? n_chunks / kShareDiv : 0;
+    const int n_static = n_chunks - n_share;
+    // GRU units and fc1 rows of this CTA
+    const int j0 = min(G, cta * p.jpc), jn = min(G, j0 + p.jpc) - j0;
+    const int f0 = min(F, cta * p.fpc), fn = min(F, f0 + p.fpc) - f0;
+
+    if (tid == 0) {
+        for (int s = 0; s < p.n_slots; ++s) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
+        }
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::fence_proxy_async();
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    // ------------------------------------------------------------------ producer
+    // Four lanes issue the ring's bulk copies in lockstep rounds: each round
+    // hands consecutive slot numbers to the lanes that have an item, so every
+    // lane keeps the same count of slots issued while the copies (and the
+    // waits for free slots) of a round proceed in parallel.
+    if (warp == kConsumerWarps) {
+        if (lane >= kProducerLanes) return;
+        constexpr unsigned kLanes = (1u << kProducerLanes) - 1u;
+        if (!full_vocab) pdl_wait();  // the pool ids come from the previous kernel
+        const uint64_t pol = full_vocab ? tc::policy_evict_normal() : tc::policy_evict_last();
+        int q = 0;        // slots issued so far (same in every lane)
+        bool ok = true;   // same in every lane
+        // fill slot number qq with rows/entries [item0, item0 + nr); item0 < 0: end of a step
+        auto issue_at = [&](int qq, long long item0, int nr) {
+            const int slot = qq % p.n_slots;
+            if (!tc::mbar_wait(empty0 + 8 * slot, (uint32_t)(((qq / p.n_slots) & 1) ^ 1), abort_flag, p.err))
+                return false;
+            srow[slot] = (int)item0;
+            if (item0 < 0) {
+                tc::mbar_arrive(full0 + 8 * slot);
+            } else {
+                const uint32_t dst = tc::smem_u32(ring + (size_t)slot * slot_bytes);
+                tc::mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)(nr * row_bytes));
+                if (full_vocab) {
+                    tc::bulk_load(dst, p.fc2 + (size_t)item0 * F, (uint32_t)(nr * row_bytes), full0 + 8 * slot, pol);
+                } else {
+                    for (int r = 0; r < nr; ++r)
+                        tc::bulk_load(dst + (uint32_t)(r * row_bytes), p.fc2 + (size_t)p.pool[item0 + r] * F,
+                                      (uint32_t)row_bytes, full0 + 8 * slot, pol);
+                }
+            }
+            return true;
+        };
+        auto round = [&](bool have, long long item0, int nr) {
+            const unsigned vm = __ballot_sync(kLanes, have);
+            bool mine = true;
+            if (have) mine = issue_at(q + __popc(vm & ((1u << lane) - 1u)), item0, nr);
+            q += __popc(vm);
+            ok = __all_sync(kLanes, mine) != 0;
+        };
+        if (p.resident) {
+            // pool rows loaded once: chunk c stays in slot c for the whole launch
+            for (int c0 = 0; c0 < n_chunks && ok; c0 += kProducerLanes) {
+                const int c = c0 + lane;
+                round(c < n_chunks, w0 + c * kRows, min(kRows, nw - c * kRows));
+            }
+        } else {
+            const unsigned total_claims = (unsigned)((p.seg / kRows) / kShareDiv + 1) * (unsigned)grid;
+            for (int k = 1; k <= p.n_corr; ++k) {
+                ok = __all_sync(kLanes, ok && !*abort_flag) != 0;
+                if (!ok) break;
+                const bool fwd = (k & 1) != 0;
+                for (int ci0 = 0; ci0 < n_static && ok; ci0 += kProducerLanes) {
+                    const int ci = ci0 + lane;
+                    const int c = fwd ? ci : n_chunks - 1 - ci;
+                    round(ci < n_static, w0 + c * kRows, min(kRows, nw - c * kRows));
+                }
+                if (full_vocab && ok) {
+                    // shared tails of every slice, kProducerLanes chunks per claim;
+                    // the counters are cleared by the run's first kernel
+                    if (k == 1) pdl_wait();
+                    unsigned* ctr = p.claim + k;
+                    unsigned base = lane == 0 ? atomicAdd(ctr, (unsigned)kProducerLanes) : 0u;
+                    base = __shfl_sync(kLanes, base, 0);
+                    while (base < total_claims && ok) {
+                        unsigned next = total_claims;  // the next claim is requested before this one is issued
+                        if (lane == 0 && base + kProducerLanes < total_claims)
+                            next = atomicAdd(ctr, (unsigned)kProducerLanes);
+                        const unsigned i = base + (unsigned)lane;
+                        bool have = false;
+                        long long item0 = 0;
+                        int nr = 0;
+                        if (i < total_claims) {
+                            const int owner = (int)(i % (unsigned)grid), j = (int)(i / (unsigned)grid);
+                            const long long ow0 = min(work, (long long)owner * p.seg);
+                            const int onw = (int)(min(work, ow0 + p.seg) - ow0);
+                            const int och = (onw + kRows - 1) / kRows, osh = och / kShareDiv;
+                            if (j < osh) {
+                                const int oc = fwd ? och - osh + j : osh - 1 - j;
+                                have = true;
+                                item0 = ow0 + oc * kRows;
+                                nr = min(kRows, onw - oc * kRows);
+                            }
+                        }
+                        round(have, item0, nr);
+                        base = __shfl_sync(kLanes, next, 0);
+                    }
+                }
+                for (int e0 = 0; e0 < p.n_cons && ok; e0 += kProducerLanes) round(e0 + lane < p.n_cons, -1, 0);
+            }
+        }
+        if (lane != 0) return;
+        // the copies issued last must land before the block may exit
+        for (int i = q > p.n_slots ? q - p.n_slots : 0; i < q; ++i) {
+            const unsigned long long t1 = tc::globaltimer();
+            while (!tc::mbar_try_wait(full0 + 8 * (i % p.n_slots), (uint32_t)((i / p.n_slots) & 1)) &&
+                   tc::globaltimer() - t1 < 2000000ull) {
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    bool failed = false;
+    const uint64_t pol_keep = tc::policy_evict_last();
+    // resident weights: this CTA's W_hh rows (3 gates x its units) and fc1 rows
+    {
+        const int per_row = G / 8;  // 16-byte pieces of a row
+        for (int i = tid; i < (p.wh_res ? 3 * jn * per_row : 0); i += kConsumerWarps * 32) {
+            const int rr = i / per_row, e = (i % per_row) * 8;
+            const int gate = rr / jn, jj = rr % jn;
+            cp_async16((void*)(swhh + ((size_t)gate * p.jpc + jj) * G + e),
+                       p.w_hh + ((size_t)gate * G + j0 + jj) * G + e);
+        }
+        for (int i = tid; i < fn * per_row; i += kConsumerWarps * 32) {
+            const int rr = i / per_row, e = (i % per_row) * 8;
+            cp_async16((void*)(sfc1 + (size_t)rr * G + e), p.fc1 + (size_t)(f0 + rr) * G + e);
+        }
+        cp_async_commit();
+    }
+    if (full_vocab)
+        for (int i = tid; i < nw; i += kConsumerWarps * 32) sbias[i] = __bfloat162float(p.bias[w0 + i]);
+
+    // W_hh row `gate*G + j0 + jj` dotted with the state of every request:
+    // from shared memory, or with the row held in registers from L2
+    auto whh_dots = [&](int gate, int jj, float* out) {
+        if (p.wh_res) {
+            const __nv_bfloat16* row = swhh + ((size_t)gate * p.jpc + jj) * G;
+            for (int b = 0; b < B; ++b) out[b] = warp_sum(smem_dot<NCH>(row, sh + b * G, G, lane));
+        } else {
+            RegRow<__nv_bfloat16, NCH> w;
+            w.load(p.w_hh + ((size_t)gate * G + j0 + jj) * G, G, lane, pol_keep);
+            for (int b = 0; b < B; ++b) out[b] = warp_sum(row_dot_smem(w, sh + b * G, G, lane));
+        }
+    };
+
+    // trace stamps (thread 0): slot s = time at the end of phase s
+    unsigned long long* tr = p.trace ? p.trace + (size_t)cta * DOMINO_TRACE_SLOTS : nullptr;
+    int ts = 0;
+    auto stamp = [&]() {
+        if (tr && tid == 0 && ts < DOMINO_TRACE_SLOTS) tr[ts] = tc::globaltimer();
+        ++ts;
+    };
+    stamp();  // 0
+
+    // token of GRU update u (1..14) for request b, from p_u; checked
+    auto fed_token = [&](int b, int u, int p_u) {
+        int t = p.forced ? p.forced[(size_t)b * kProposals + (u - 1)] : p_u;
+        if (t < 0 || t >= V) {
+            if (cta == 0) {
+                p.bad[b] = 1;
+                atomicOr(p.err, kErrBadToken);
+            }
+            t = 0;
+        }
+        return t;
+    };
+
+    // ---- seed update 0 (h_{-1} = 0): the verified token only, independent
+    // of the previous kernel; every CTA computes the whole state
+    if (tid < B) {
+        int t = p.verified[tid];
+        if (t < 0 || t >= V) {
+            if (cta == 0) {
+                p.bad[tid] = 1;
+                atomicOr(p.err, kErrBadToken);
+            }
+            t = 0;
+        }
+        stok[tid] = t;
+    }
+    cons_sync();
+    for (int i = tid; i < B * G; i += kConsumerWarps * 32) {
+        const int b = i / G, j = i % G;
+        const float* gi = p.gi_table + (size_t)stok[b] * 3 * G + j;
+        // h = 0: the reset gate multiplies W_hn h = 0 and drops out
+        const float zg = sigmoidf_(__ldg(gi + G));
+        const float n = tanhf(__ldg(gi + 2 * G));
+        const float h = (1.f - zg) * n;
+        sh[b * G + j] = h;
+        if (p.dbg_h && j >= j0 && j < j0 + jn) p.dbg_h[((size_t)b * kProposals + 0) * G + j] = h;
+    }
+    cp_async_wait_all();
+    cons_sync();
+    // hidden-side products of update 1 for this CTA's units, kept until the
+    // run's tag is known
+    for (int it = warp; it < 3 * jn; it += kConsumerWarps) {
+        const int gate = it / jn, jj = it % jn;
+        float v[kLLMaxBatch];
+        whh_dots(gate, jj, v);
+        if (lane == 0)
+            for (int b = 0; b < B; ++b) sgh0[(b * 3 + gate) * p.jpc + jj] = v[b];
+    }
+    stamp();  // 1
+    pdl_wait();  // base logits, p_1 and the pool are ready; the run counter is bumped
+    const unsigned ep16 = *p.epoch * 16u;
+    int pub = 0;  // publications so far (for the timeout test hook)
+    // the buffers of update u / step k
+    auto xgh_of = [&](int u) { return p.xgh + (size_t)(u & 1) * kLLMaxBatch * 3 * G; };
+    auto xa_of = [&](int k) { return p.xa + (size_t)(k & 1) * kLLMaxBatch * F; };
+    auto xbest_of = [&](int k) { return p.xbest + (size_t)(k & 1) * grid * kLLMaxBatch; };
+    auto publish_ok = [&]() { return !(cta == 0 && ++pub == p.drop_at); };
+    cons_sync();
+    if (publish_ok())
+        for (int i = tid; i < B * 3 * jn; i += kConsumerWarps * 32) {
+            const int b = i / (3 * jn), r = i % (3 * jn), gate = r / jn, jj = r % jn;
+            st_relaxed_u64(xgh_of(1) + (size_t)b * 3 * G + gate * G + j0 + jj,
+                           tagged(sgh0[(b * 3 + gate) * p.jpc + jj], ep16 + 1));
+        }
+    if (!full_vocab)
+        for (int i = tid; i < nw; i += kConsumerWarps * 32) {
+            const int v = p.pool[w0 + i];
+            spid[i] = v;
+            sbias[i] = __bfloat162float(p.bias[v]);
+            // the candidates' token-table rows: every fed token of a pool run is one of them
+            if (p.pin_gi) tc::bulk_prefetch_l2(p.gi_table + (size_t)v * 3 * G, (uint32_t)(3 * G * 4), pol_keep);
+        }
+    // this CTA's entries of s (they may come from the previous kernel)
+    for (int i = tid; i < B * kProposals * fn; i += kConsumerWarps * 32) {
+        const int b = i / (kProposals * fn), r = i % (kProposals * fn), j = r / fn, f = r % fn;
+        ss[(b * kProposals + j) * p.fpc + f] = __bfloat162float(p.s[((size_t)b * kProposals + j) * F + f0 + f]);
+    }
+
+    // ---- GRU update u: every CTA rebuilds the whole state in sh from the
+    // token-table row of the fed token and the published hidden-side products
+    auto gru_update = [&](int u) {
+        const unsigned tag = ep16 + (unsigned)u;
+        constexpr int kPer = 3;
+        constexpr int kNT = kConsumerWarps * 32;
+        for (int base = 0; base < B * G; base += kPer * kNT) {
+            float gi[kPer][3];
+            unsigned long long gh[kPer][3];
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {  // every load of the round before any use
+                const int i = base + e * kNT + tid;
+                if (i < B * G) {
+                    const int b = i / G, j = i % G;
+                    const float* g = p.gi_table + (size_t)stok[b] * 3 * G + j;
+                    const unsigned long long* x = xgh_of(u) + (size_t)b * 3 * G + j;
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        gi[e][q] = __ldg(g + q * G);
+                        gh[e][q] = ld_relaxed_u64(x + q * G);
+                    }
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                const int i = base + e * kNT + tid;
+                if (i < B * G) {
+                    const int b = i / G, j = i % G;
+                    const unsigned long long* x = xgh_of(u) + (size_t)b * 3 * G + j;
+                    float hv[3];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        const unsigned long long w = poll_word(
+                            x + q * G, gh[e][q], [&](unsigned long long v) { return (unsigned)(v >> 32) == tag; },
+                            abort_flag, p.err, failed);
+                        hv[q] = __uint_as_float((unsigned)w);
+                    }
+                    const float r = sigmoidf_(gi[e][0] + hv[0]);
+                    const float zg = sigmoidf_(gi[e][1] + hv[1]);
+                    const float n = tanhf(gi[e][2] + r * hv[2]);
+                    const float h = (1.f - zg) * n + zg * sh[b * G + j];
+                    sh[b * G + j] = h;
+                    if (p.dbg_h && j >= j0 && j < j0 + jn) p.dbg_h[((size_t)b * kProposals + u) * G + j] = h;
+                }
+            }
+        }
+    };
+
+    // update 1 consumes p_1 (the LM-head's argmax of base row 1)
+    if (tid < B) stok[tid] = fed_token(tid, 1, (int)key_index(__ldcg(&p.keys[(size_t)tid * kBlock])));
+    cons_sync();
+    gru_update(1);
+    if (cons_sync_or(failed)) return;
+    stamp();  // 2
+
+    float areg[NCH][8];
+    int areg_b = -1;
+    auto load_areg = [&](int b) {
+#pragma unroll
+        for (int cc = 0; cc < NCH; ++cc) {
+            const int e = (lane + 32 * cc) * 8;
+            if (e < F) lds8(sa + b * F + e, areg[cc]);
+        }
+        areg_b = b;
+    };
+    // the rows of one slot (entries item0 .. item0+nr-1) dotted with the
+    // activations of their request(s); lane-partial sums in part[]
+    auto slot_dots = [&](const __nv_bfloat16* srows, long long item0, int nr, float* part) {
+        const int bl0 = full_vocab ? 0 : (int)(item0 / p.K);
+        const int bl1 = full_vocab ? 0 : (int)((item0 + nr - 1) / p.K);
+        if (bl0 == bl1) {
+            if (bl0 != areg_b) load_areg(bl0);
+            float acc[kRows][2];
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) acc[rr][0] = acc[rr][1] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NCH; ++cc) {
+                const int e = (lane + 32 * cc) * 8;
+                if (e < F) {
+#pragma unroll
+                    for (int rr = 0; rr < kRows; ++rr) {
+                        if (rr < nr) {
+                            float wv[8];
+                            lds8(srows + (size_t)rr * F + e, wv);
+#pragma unroll
+                            for (int i = 0; i < 8; i += 2) {
+                                acc[rr][0] = fmaf(wv[i], areg[cc][i], acc[rr][0]);
+                                acc[rr][1] = fmaf(wv[i + 1], areg[cc][i + 1], acc[rr][1]);
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) part[rr] = acc[rr][0] + acc[rr][1];
+        } else {  // a slot across a request boundary of the pool
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) {
+                part[rr] = 0.f;
+                if (rr < nr) {
+                    const int bl = (int)((item0 + rr) / p.K);
+                    if (bl != areg_b) load_areg(bl);
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < NCH; ++cc) {
+                        const int e = (lane + 32 * cc) * 8;
+                        if (e < F) {
+                            float wv[8];
+                            lds8(srows + (size_t)rr * F + e, wv);
+#pragma unroll
+                            for (int i = 0; i < 8; i += 2) {
+                                a0 = fmaf(wv[i], areg[cc][i], a0);
+                                a1 = fmaf(wv[i + 1], areg[cc][i + 1], a1);
+                            }
+                        }
+                    }
+                    part[rr] = a0 + a1;
+                }
+            }
+        }
+    };
+    // best word of an exchange: orderable value, then ~id (lower id wins), then the step
+    auto best_key = [](float c, int v) {
+        return ((unsigned long long)ord_f32(c) << 32) |
+               ((unsigned long long)(~(uint32_t)v & 0x3FFFFu) << kBestIdShift);
+    };
+    // per-request maxima of this thread's m[] over the CTA into sred[15*kLLMaxBatch + b]
+    auto block_max = [&](unsigned long long* m) {
+        for (int b = 0; b < B; ++b) {
+            const unsigned long long w = warp_max_u64(m[b]);
+            if (lane == 0) sred[warp * kLLMaxBatch + b] = w;
+        }
+        cons_sync();
+        if (tid < B) {
+            unsigned long long w = 0ull;
+            for (int i = 0; i < kConsumerWarps; ++i) w = max(w, sred[i * kLLMaxBatch + tid]);
+            sred[kConsumerWarps * kLLMaxBatch + tid] = w;
+        }
+        cons_sync();
+    };
+
+    const int rsel = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);  // the slot row this lane finishes
+    int qw = warp;  // ring: sequence number of this warp's next slot (slot q is consumed by warp q % n_cons)
+    for (int k = 1; k <= p.n_corr; ++k) {
+        const unsigned tag_k = ep16 + (unsigned)k;
+        const bool fwd = (k & 1) != 0;
+        // rows of the slice this CTA finishes itself (full vocabulary: the
+        // static part, whose end alternates with the walking direction)
+        const int st_lo = full_vocab ? (fwd ? 0 : n_share * kRows) : 0;
+        const int st_hi = full_vocab ? (fwd ? min(nw, n_static * kRows) : nw) : nw;
+        for (int r = st_lo + tid; r < st_hi; r += kConsumerWarps * 32) {
+            const long long item = w0 + r;
+            const int b = full_vocab ? 0 : (int)(item / p.K);
+            const int v = full_vocab ? (int)item : spid[r];
+            cp_async4(&sL[r], p.L + ((size_t)b * kBlock + kRowOffset + k) * V + v);
+        }
+        cp_async_commit();
+
+        // ---- P_k: the projector slice (published first), then the next
+        // update's hidden-side products of this CTA's units
+        {
+            const bool pub_a = publish_ok();
+            const bool pub_g = k < p.n_corr && publish_ok();
+            const int n_items = fn + (k < p.n_corr ? 3 * jn : 0);
+            for (int it = warp; it < n_items; it += kConsumerWarps) {
+                if (it < fn) {
+                    const __nv_bfloat16* row = sfc1 + (size_t)it * G;
+                    for (int b = 0; b < B; ++b) {
+                        const float v = warp_sum(smem_dot<NCH>(row, sh + b * G, G, lane));
+                        if (lane == 0) {
+                            const int f = f0 + it;
+                            const float z = v + ss[(b * kProposals + k) * p.fpc + it];
+                            if (pub_a) st_relaxed_u64(xa_of(k) + (size_t)b * F + f, tagged(z * sigmoidf_(z), tag_k));
+                            if (p.dbg_z) p.dbg_z[((size_t)b * kCorrected + (k - 1)) * F + f] = z;
+                        }
+                    }
+                } else {
+                    const int g = it - fn, gate = g / jn, jj = g % jn;
+                    float v[kLLMaxBatch];
+                    whh_dots(gate, jj, v);
+                    if (lane == 0 && pub_g)
+                        for (int b = 0; b < B; ++b)
+                            st_relaxed_u64(xgh_of(k + 1) + (size_t)b * 3 * G + gate * G + j0 + jj,
+                                           tagged(v[b], ep16 + (unsigned)(k + 1)));
+                }
+            }
+        }
+        stamp();  // 3 + 4(k-1): projector published
+        // ---- C_k: all activations, then this CTA's slice
+        {
+            constexpr int kNT = kConsumerWarps * 32;
+            const unsigned long long* xa = xa_of(k);
+            for (int base = 0; base < B * F; base += 4 * kNT) {
+                unsigned long long w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = base + e * kNT + tid;
+                    w[e] = i < B * F ? ld_relaxed_u64(xa + i) : 0ull;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = base + e * kNT + tid;
+                    if (i < B * F)
+                        sa[i] = __uint_as_float((unsigned)poll_word(
+                            xa + i, w[e], [&](unsigned long long v) { return (unsigned)(v >> 32) == tag_k; },
+                            abort_flag, p.err, failed));
+                }
+            }
+        }
+        cp_async_wait_all();
+        if (cons_sync_or(failed)) return;
+        areg_b = -1;
+        stamp();  // 4 + 4(k-1): activations in
+        unsigned long long best_direct = 0ull;  // shared rows finished in the slot loop (full vocabulary)
+        if (p.resident) {
+            for (int c = warp; c < n_chunks; c += kConsumerWarps) {
+                if (k == 1 && !tc::mbar_wait(full0 + 8 * c, 0u, abort_flag, p.err)) {
+                    failed = true;
+                    break;
+                }
+                const int nr = min(kRows, nw - c * kRows);
+                float part[kRows];
+                slot_dots(reinterpret_cast<const __nv_bfloat16*>(ring + (size_t)c * slot_bytes), w0 + c * kRows, nr,
+                          part);
+                const float tot = warp_sum4(part[0], part[1], part[2], part[3], lane);
+                if ((lane & 7) == 0 && rsel < nr) stot[c * kRows + rsel] = tot;
+            }
+        } else if (warp < p.n_cons) {
+            while (true) {
+                const int q = qw;
+                qw += p.n_cons;
+                const int slot = q % p.n_slots;
+                if (!tc::mbar_wait(full0 + 8 * slot, (uint32_t)((q / p.n_slots) & 1), abort_flag, p.err)) {
+                    failed = true;
+                    break;
+                }
+                const int item0 = srow[slot];
+                if (item0 < 0) {  // end of this step for this warp
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
+                    break;
+                }
+                const int nr = full_vocab ? min(kRows, V - item0) : min(kRows, (int)(w1 - item0));
+                const bool own = item0 >= w0 + st_lo && item0 < w0 + st_hi;
+                // a shared row: this lane fetches its bias and base logit before the dots
+                float tail = 0.f;
+                if (!own && (lane & 7) == 0 && rsel < nr)
+                    tail = __bfloat162float(p.bias[item0 + rsel]) +
+                           __ldg(p.L + (size_t)(kRowOffset + k) * V + item0 + rsel);
+                float part[kRows];
+                slot_dots(reinterpret_cast<const __nv_bfloat16*>(ring + (size_t)slot * slot_bytes), item0, nr, part);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);  // the slot is read
+                const float tot = warp_sum4(part[0], part[1], part[2], part[3], lane);
+                if ((lane & 7) == 0 && rsel < nr) {
+                    if (own) {
+                        stot[item0 - w0 + rsel] = tot;
+                    } else {
+                        const float cv = tot + tail;
+                        best_direct = max(best_direct, best_key(cv, item0 + rsel));
+                        if (p.dbg_scores) p.dbg_scores[(size_t)(k - 1) * V + item0 + rsel] = cv;
+                    }
+                }
+            }
+        }
+        if (cons_sync_or(failed)) return;
+        // ---- finish this CTA's rows: bias, base logit, per-request best
+        {
+            unsigned long long m[kLLMaxBatch];
+#pragma unroll
+            for (int b = 0; b < kLLMaxBatch; ++b) m[b] = 0ull;
+            m[0] = best_direct;
+            for (int r = st_lo + tid; r < st_hi; r += kConsumerWarps * 32) {
+                const long long item = w0 + r;
+                const int b = full_vocab ? 0 : (int)(item / p.K);
+                const int v = full_vocab ? (int)item : spid[r];
+                const float cv = stot[r] + sbias[r] + sL[r];
+                const unsigned long long key = best_key(cv, v);
+#pragma unroll
+                for (int bb = 0; bb < kLLMaxBatch; ++bb)
+                    if (bb == b) m[bb] = max(m[bb], key);
+                if (p.dbg_scores) {
+                    if (full_vocab) p.dbg_scores[(size_t)(k - 1) * V + v] = cv;
+                    else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
+                }
+            }
+            block_max(m);
+            const bool pub_b = publish_ok();
+            if (tid < B && pub_b)
+                st_relaxed_u64(xbest_of(k) + (size_t)cta * kLLMaxBatch + tid,
+                               sred[kConsumerWarps * kLLMaxBatch + tid] | (unsigned long long)k);
+        }
+        stamp();  // 5 + 4(k-1): best published
+        if (k == p.n_corr && cta != 0) return;  // only CTA 0 reports the last step
+        // ---- every CTA's best of step k: p_{k+1} for every request
+        {
+            unsigned long long m[kLLMaxBatch];
+#pragma unroll
+            for (int b = 0; b < kLLMaxBatch; ++b) m[b] = 0ull;
+            const unsigned kk = (unsigned)k;
+            for (int i = tid; i < grid * B; i += kConsumerWarps * 32) {
+                const int c = i / B, b = i % B;
+                const unsigned long long* x = xbest_of(k) + (size_t)c * kLLMaxBatch + b;
+                const unsigned long long w = poll_word(
+                    x, ld_relaxed_u64(x), [&](unsigned long long v) { return (unsigned)(v & kBestTagMask) == kk; },
+                    abort_flag, p.err, failed);
+#pragma unroll
+                for (int bb = 0; bb < kLLMaxBatch; ++bb)
+                    if (bb == b) m[bb] = max(m[bb], w & ~(unsigned long long)kBestTagMask);
+            }
+            block_max(m);
+            if (tid < B) {
+                const unsigned long long w = sred[kConsumerWarps * kLLMaxBatch + tid];
+                const int id = (int)(~(uint32_t)(w >> kBestIdShift) & 0x3FFFFu);
+                if (cta == 0) p.keys[(size_t)tid * kBlock + k] = pack_key(unord_f32((uint32_t)(w >> 32)), (uint32_t)id);
+                if (k < p.n_corr) stok[tid] = fed_token(tid, k + 1, id);
+            }
+        }
+        if (cons_sync_or(failed)) return;
+        if (k < p.n_corr) {
+            gru_update(k + 1);
+            if (cons_sync_or(failed)) return;
+        }
+        stamp();  // 6 + 4(k-1): next state built
+    }
+}
+
+
+struct LLPlan {
+    int seg, jpc, fpc, n_slots, n_cons, resident, wh_res, smem;
+};
+
+LLPlan make_ll_plan(const domino_ctx* c, int B, int K) {
+    const domino_config& g = c->cfg;
+    const int grid = c->num_sms;
+    const long long work = K == 0 ? (long long)g.V : (long long)B * K;
+    LLPlan pl{};
+    pl.seg = (int)((work + grid - 1) / grid);
+    pl.seg = (pl.seg + kRows - 1) / kRows * kRows;
+    pl.jpc = (g.G + grid - 1) / grid;
+    pl.fpc = (g.F + grid - 1) / grid;
+    const int slot_bytes = kRows * g.F * 2;
+    int max_smem = 0;
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    // over the full vocabulary the correction phase leaves the hidden-side
+    // products plenty of time to read W_hh from L2, and the ring gets the room
+    pl.wh_res = K > 0;
+    const LLLayout base(0, slot_bytes, g.G, g.F, pl.jpc, pl.fpc, pl.seg, B, pl.wh_res != 0);
+    const int avail = max_smem - base.total - 1024;
+    const int per_slot = slot_bytes + 20;
+    const int chunks = pl.seg / kRows;
+    if (K > 0 && chunks * per_slot <= avail && chunks <= kMaxSlots) {
+        pl.resident = 1;  // pool rows loaded once
+        pl.n_slots = chunks;
+        pl.n_cons = kConsumerWarps;
+    } else {
+        int n = avail / per_slot;
+        if (n > kMaxSlots) n = kMaxSlots;
+        // consumer warps: the count whose multiple uses the most of the ring (at least 8);
+        // slot q is consumed by warp q % n_cons
+        int best = 0, nc = 0;
+        for (int w = kConsumerWarps; w >= 8; --w)
+            if (n / w * w > best) {
+                best = n / w * w;
+                nc = w;
+            }
+        pl.n_slots = best;
+        pl.n_cons = nc;
+    }
+    if (pl.n_slots < 1) return pl;
+    pl.smem = LLLayout(pl.n_slots, slot_bytes, g.G, g.F, pl.jpc, pl.fpc, pl.seg, B, pl.wh_res != 0).total;
+    return pl;
+}
+
+}  // namespace
+
+// One request over the full vocabulary, or pools of up to kLLMaxBatch
+// requests; bf16 rows of at most 1024 elements, ids that fit the 18 id bits
+// of an exchange word, and a slice that fits the per-CTA tables.
+bool persist_ll_supported(const domino_ctx* c, const RunArgs& r) {
+    const domino_config& g = c->cfg;
+    if (g.dtype != DOMINO_DTYPE_BF16 || !c->xbest) return false;
+    if (g.G > 1024 || g.F > 1024 || (g.G & 7) || (g.F & 7)) return false;
+    if (g.V >= (1 << 18) || r.B < 1 || r.B > kLLMaxBatch) return false;
+    if (r.K == 0 && r.B != 1) return false;
+    const LLPlan pl = make_ll_plan(c, r.B, r.K);
+    if (pl.seg > kMaxSeg || pl.jpc > 64 || pl.fpc > 64) return false;
+    if (pl.resident) return pl.smem > 0;
+    return pl.n_slots >= 8 && pl.smem > 0;
+}
+
+cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r) {
+    const domino_config& g = c->cfg;
+    const LLPlan pl = make_ll_plan(c, r.B, r.K);
+    LLParams p;
+    p.w_hh = (const __nv_bfloat16*)c->w_hh;
+    p.fc1 = (const __nv_bfloat16*)c->fc1;
+    p.fc2 = (const __nv_bfloat16*)c->fc2;
+    p.bias = (const __nv_bfloat16*)c->bias;
+    p.s = (const __nv_bfloat16*)r.s;
+    p.gi_table = c->gi_table;
+    p.verified = r.verified;
+    p.forced = r.forced;
+    p.pool = c->pool;
+    p.L = c->L;
+    p.keys = c->keys;
+    p.bad = c->bad;
+    p.err = c->err;
+    p.claim = c->sync + kClaimCounters;
+    p.epoch = c->sync + kRunEpochWord;
+    p.xa = c->xa;
+    p.xgh = c->xgh;
+    p.xbest = c->xbest;
+    p.dbg_h = r.dbg.h;
+    p.dbg_z = r.dbg.z;
+    p.dbg_scores = r.dbg.scores;
+    p.trace = r.dbg.trace;
+    p.B = r.B;
+    p.K = r.K;
+    p.V = g.V;
+    p.G = g.G;
+    p.F = g.F;
+    p.n_corr = r.n_prop - 1;
+    p.seg = pl.seg;
+    p.jpc = pl.jpc;
+    p.fpc = pl.fpc;
+    p.n_slots = pl.n_slots;
+    p.n_cons = pl.n_cons;
+    p.resident = pl.resident;
+    p.wh_res = pl.wh_res;
+    // the candidates' token-table rows stay in L2 when they are a modest share of it
+    p.pin_gi = r.K > 0 && (long long)r.B * r.K * 3 * g.G * 4 <= (48ll << 20);
+    p.drop_at = c->drop_barrier;  // one-shot test hook
+    c->drop_barrier = 0;
+
+    const int mx = g.G > g.F ? g.G : g.F;
+    void (*kern)(LLParams) = mx <= 256 ? k_rollout_ll<1> : mx <= 512 ? k_rollout_ll<2> : k_rollout_ll<4>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c->num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = r.st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    ++r.launches;
+    return e;
+}
+
+}  // namespace domino

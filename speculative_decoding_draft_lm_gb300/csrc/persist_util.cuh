@@ -1,0 +1,154 @@
+// Device helpers shared by the persistent drivers of the rollout: the
+// consumer-warp barrier, asynchronous 4-byte copies, shared-memory and
+// register-held weight rows widened to fp32, and transposed warp sums.
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace domino {
+namespace persist {
+
+// 15 consumer warps + 1 producer warp: the consumers synchronise among
+// themselves on named barrier 1
+constexpr int kConsumerWarps = 15;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 480;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// 8 consecutive elements of a shared-memory row widened to fp32
+__device__ __forceinline__ void lds8(const float* p, float* o) {
+    float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w; o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+}
+__device__ __forceinline__ void lds8(const __nv_bfloat16* p, float* o) {
+    uint4 q = *reinterpret_cast<const uint4*>(p);
+    bf16x2_to_f32(q.x, o[0], o[1]);
+    bf16x2_to_f32(q.y, o[2], o[3]);
+    bf16x2_to_f32(q.z, o[4], o[5]);
+    bf16x2_to_f32(q.w, o[6], o[7]);
+}
+
+// One weight row held in registers: lane l owns elements (l + 32 c) * 8 .. +7
+// for c < NCH (NCH * 256 >= row length).  All chunks are requested before any
+// is used, with an L2 evict-last hint (these small matrices are re-read every
+// step while fc2 streams past them).
+template <typename T, int NCH>
+struct RegRow;
+template <int NCH>
+struct RegRow<__nv_bfloat16, NCH> {
+    uint4 q[NCH];
+    __device__ __forceinline__ void load(const __nv_bfloat16* row, int n, int lane, uint64_t pol) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int e = (lane + 32 * c) * 8;
+            if (e < n)
+                asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                             : "=r"(q[c].x), "=r"(q[c].y), "=r"(q[c].z), "=r"(q[c].w)
+                             : "l"(row + e), "l"(pol));
+            else
+                q[c] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    __device__ __forceinline__ void get(int c, float* o) const {
+        bf16x2_to_f32(q[c].x, o[0], o[1]);
+        bf16x2_to_f32(q[c].y, o[2], o[3]);
+        bf16x2_to_f32(q[c].z, o[4], o[5]);
+        bf16x2_to_f32(q[c].w, o[6], o[7]);
+    }
+};
+template <int NCH>
+struct RegRow<float, NCH> {
+    float4 q[2 * NCH];
+    __device__ __forceinline__ void load(const float* row, int n, int lane, uint64_t pol) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int e = (lane + 32 * c) * 8;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (e < n)
+                    asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                                 : "=f"(q[2 * c + h].x), "=f"(q[2 * c + h].y), "=f"(q[2 * c + h].z),
+                                   "=f"(q[2 * c + h].w)
+                                 : "l"(row + e + 4 * h), "l"(pol));
+                else
+                    q[2 * c + h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+    __device__ __forceinline__ void get(int c, float* o) const {
+        o[0] = q[2 * c].x; o[1] = q[2 * c].y; o[2] = q[2 * c].z; o[3] = q[2 * c].w;
+        o[4] = q[2 * c + 1].x; o[5] = q[2 * c + 1].y; o[6] = q[2 * c + 1].z; o[7] = q[2 * c + 1].w;
+    }
+};
+
+// dot of a register row with a shared-memory fp32 vector (same element map)
+template <typename T, int NCH>
+__device__ __forceinline__ float row_dot_smem(const RegRow<T, NCH>& w, const float* x, int n, int lane) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int e = (lane + 32 * c) * 8;
+        if (e < n) {
+            float ww[8], xx[8];
+            w.get(c, ww);
+            lds8(x + e, xx);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                a0 = fmaf(ww[i], xx[i], a0);
+                a1 = fmaf(ww[i + 1], xx[i + 1], a1);
+            }
+        }
+    }
+    return a0 + a1;
+}
+
+// Sum each of 4 per-lane values over the warp with 6 shuffles (a transposed
+// butterfly).  Lane l ends with the total of value ((l >> 4) & 1) * 2 +
+// ((l >> 3) & 1).
+__device__ __forceinline__ float warp_sum4(float v0, float v1, float v2, float v3, int lane) {
+    const bool hi16 = (lane & 16) != 0;
+    float a = hi16 ? v2 : v0, b = hi16 ? v3 : v1;          // keep
+    float c = hi16 ? v0 : v2, d = hi16 ? v1 : v3;          // send
+    a += __shfl_xor_sync(0xffffffffu, c, 16);
+    b += __shfl_xor_sync(0xffffffffu, d, 16);
+    const bool hi8 = (lane & 8) != 0;
+    float keep = hi8 ? b : a, send = hi8 ? a : b;
+    keep += __shfl_xor_sync(0xffffffffu, send, 8);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+    return keep;
+}
+
+// 16-byte asynchronous global -> shared copy (both 16-byte aligned)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Named-barrier sync of the consumer warps that also ORs a predicate over
+// them: every thread gets the same answer, so a decision taken on it (e.g.
+// to stop after a timed-out wait) is uniform.
+__device__ __forceinline__ bool cons_sync_or(bool x) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 480, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)x)
+        : "memory");
+    return r != 0;
+}
+
+}  // namespace persist
+}  // namespace domino

@@ -31,6 +31,7 @@ DOMINO_BLOCK = 16
 DOMINO_DRIVER_AUTO = 0
 DOMINO_DRIVER_KERNELS = 1
 DOMINO_DRIVER_PERSISTENT = 2
+DOMINO_DRIVER_PERSISTENT_GRID = 3
 
 # every symbol the header declares
 EXPORTED = (

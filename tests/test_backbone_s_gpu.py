@@ -49,7 +49,7 @@ def test_small_in_library_s(dtype, B, K):
 def test_small_in_library_s_both_drivers():
     from speculative_decoding_draft_lm_gb300 import rollout as R
     sh = inputs.small_shape(dtype="bf16")
-    for drv in (R.DOMINO_DRIVER_KERNELS, R.DOMINO_DRIVER_PERSISTENT):
+    for drv in (R.DOMINO_DRIVER_KERNELS, R.DOMINO_DRIVER_PERSISTENT, R.DOMINO_DRIVER_PERSISTENT_GRID):
         _run(sh, 1, 0, scales=_scales(sh), hid_scale=0.1, driver=drv)
 
 

@@ -1,5 +1,6 @@
-"""The two drivers of the 14 dependent steps (one launch per phase, and the
-persistent cooperative kernel) agree with the oracle and with each other."""
+"""The drivers of the 14 dependent steps (one launch per phase, and the two
+persistent cooperative kernels: tagged data exchanges or grid barriers) agree
+with the oracle and with each other."""
 import numpy as np
 import pytest
 
@@ -30,7 +31,8 @@ def test_persistent_matches_kernels_and_oracle(dtype, B, K):
     eng = make_engine(sh, max_B=B, max_K=K, dw=device_weights(w))
     dreq = device_requests(r)
     outs = {}
-    for drv in (R.DOMINO_DRIVER_KERNELS, R.DOMINO_DRIVER_PERSISTENT):
+    persistent = (R.DOMINO_DRIVER_PERSISTENT, R.DOMINO_DRIVER_PERSISTENT_GRID)
+    for drv in (R.DOMINO_DRIVER_KERNELS,) + persistent:
         eng.set_driver(drv)
         g = gpu_debug(eng, sh, dreq, B, K, o["tokens"], want_scores=True)
         check_against_oracle(ow, o, g, sh, K)
@@ -39,16 +41,17 @@ def test_persistent_matches_kernels_and_oracle(dtype, B, K):
         assert eng.status() == 0
         outs[drv] = (g, free.cpu().numpy())
     gk, fk = outs[R.DOMINO_DRIVER_KERNELS]
-    gp, fp = outs[R.DOMINO_DRIVER_PERSISTENT]
     tol = TOL[dtype]
-    np.testing.assert_allclose(gp["h"], gk["h"], rtol=0, atol=tol)
-    np.testing.assert_allclose(gp["z"], gk["z"], rtol=0, atol=tol)
-    # free-running chains agree wherever the oracle's decision is not a near tie
-    for b in range(B):
-        for j in range(15):
-            if o["margin"][b, j] <= tol:
-                break
-            assert fp[b, j] == fk[b, j] == o["tokens"][b, j]
+    for drv in persistent:
+        gp, fp = outs[drv]
+        np.testing.assert_allclose(gp["h"], gk["h"], rtol=0, atol=tol)
+        np.testing.assert_allclose(gp["z"], gk["z"], rtol=0, atol=tol)
+        # free-running chains agree wherever the oracle's decision is not a near tie
+        for b in range(B):
+            for j in range(15):
+                if o["margin"][b, j] <= tol:
+                    break
+                assert fp[b, j] == fk[b, j] == o["tokens"][b, j]
     eng.close()
 
 
@@ -60,12 +63,13 @@ def test_persistent_repeat_runs_are_identical():
     w = cached_weights(sh, 0, sc)
     r = inputs.make_requests(sh, [77])
     eng = make_engine(sh, max_B=1, max_K=100, dw=device_weights(w))
-    eng.set_driver(R.DOMINO_DRIVER_PERSISTENT)
     dreq = device_requests(r)
-    for K in (0, 100):
-        a = eng.run(*dreq, K=K).cpu().numpy()
-        b = eng.run(*dreq, K=K).cpu().numpy()
-        assert (a == b).all()
+    for drv in (R.DOMINO_DRIVER_PERSISTENT, R.DOMINO_DRIVER_PERSISTENT_GRID):
+        eng.set_driver(drv)
+        for K in (0, 100):
+            a = eng.run(*dreq, K=K).cpu().numpy()
+            b = eng.run(*dreq, K=K).cpu().numpy()
+            assert (a == b).all()
     eng.close()
 
 
@@ -79,5 +83,7 @@ def test_persistent_driver_rejects_unsupported_batch():
     hid, s, ver = device_requests(r)
     out = torch.empty((4, 15), dtype=torch.int32, device="cuda")
     # full vocabulary with B > 1 runs on the tensor-core kernels instead
+    assert R.domino_rollout_run(eng.ctx, hid, s, ver, 4, 0, out) == R.DOMINO_ERR_UNSUPPORTED
+    eng.set_driver(R.DOMINO_DRIVER_PERSISTENT_GRID)
     assert R.domino_rollout_run(eng.ctx, hid, s, ver, 4, 0, out) == R.DOMINO_ERR_UNSUPPORTED
     eng.close()

@@ -58,7 +58,7 @@ def test_early_stop_matches_full_prefix(dtype, B, K):
     dreq = device_requests(r)
     drivers = [R.DOMINO_DRIVER_KERNELS]
     if K > 0 or B == 1:
-        drivers.append(R.DOMINO_DRIVER_PERSISTENT)
+        drivers += [R.DOMINO_DRIVER_PERSISTENT, R.DOMINO_DRIVER_PERSISTENT_GRID]
     for drv in drivers:
         eng.set_driver(drv)
         eng.set_proposals(15)

@@ -98,8 +98,8 @@ def test_feedback_changes_tokens(sh, B, K):
 
 @pytest.mark.parametrize("B,K", [(1, 0), (3, 2048)])
 def test_persistent_and_per_phase_states_agree_tightly(B, K):
-    """The persistent driver's merged GRU update (each CTA rebuilds the state
-    from hidden-side products other CTAs wrote) against the per-phase kernels,
+    """The persistent drivers' GRU updates (each CTA rebuilds the state from
+    hidden-side products other CTAs wrote) against the per-phase kernels,
     teacher-forced on one chain: both keep the state in fp32, so they agree far
     inside the bf16 tolerance at every one of the 15 updates."""
     from speculative_decoding_draft_lm_gb300 import rollout as R
@@ -108,13 +108,14 @@ def test_persistent_and_per_phase_states_agree_tightly(B, K):
     eng = make_engine(Q8, max_B=B, max_K=K, dw=device_weights(w))
     dreq = device_requests(r)
     got = {}
-    for drv in (R.DOMINO_DRIVER_KERNELS, R.DOMINO_DRIVER_PERSISTENT):
+    persistent = (R.DOMINO_DRIVER_PERSISTENT, R.DOMINO_DRIVER_PERSISTENT_GRID)
+    for drv in (R.DOMINO_DRIVER_KERNELS,) + persistent:
         eng.set_driver(drv)
         got[drv] = gpu_debug(eng, Q8, dreq, B, K, o["tokens"])
         check_against_oracle(ow, o, got[drv], Q8, K)
-    hk, hp = got[R.DOMINO_DRIVER_KERNELS]["h"], got[R.DOMINO_DRIVER_PERSISTENT]["h"]
-    zk, zp = got[R.DOMINO_DRIVER_KERNELS]["z"], got[R.DOMINO_DRIVER_PERSISTENT]["z"]
+    hk, zk = got[R.DOMINO_DRIVER_KERNELS]["h"], got[R.DOMINO_DRIVER_KERNELS]["z"]
     assert np.abs(hk).max() > 0.2
-    np.testing.assert_allclose(hp, hk, rtol=0, atol=1e-4)
-    np.testing.assert_allclose(zp, zk, rtol=0, atol=1e-4)
+    for drv in persistent:
+        np.testing.assert_allclose(got[drv]["h"], hk, rtol=0, atol=1e-4)
+        np.testing.assert_allclose(got[drv]["z"], zk, rtol=0, atol=1e-4)
     eng.close()

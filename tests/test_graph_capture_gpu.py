@@ -1,7 +1,9 @@
 """run() is asynchronous and makes no host synchronisation, so a whole block
-rollout can be captured in a CUDA graph and replayed: the persistent driver
-(cooperative + programmatic dependent launch), the batched per-phase driver
-with the cluster pool selection, and the tensor-core GRU path."""
+rollout can be captured in a CUDA graph and replayed: the persistent drivers
+(cooperative + programmatic dependent launch; the tagged-exchange one draws
+its tags from a run counter in device memory, so replays do not reuse them),
+the batched per-phase driver with the cluster pool selection, and the
+tensor-core GRU path."""
 import numpy as np
 import pytest
 
@@ -17,10 +19,11 @@ def _scales(sh):
     return (("emb", 1.0), ("w_ih", sh.E ** -0.5), ("w_hh", sh.G ** -0.5), ("fc1", 0.5 * sh.G ** -0.5), ("fc2", 0.2))
 
 
-@pytest.mark.parametrize("B,K", [(1, 0), (1, 100), (3, 100), (16, 0)])
-def test_captured_rollout_replays_like_eager(B, K):
+@pytest.mark.parametrize("B,K,driver", [(1, 0, 0), (1, 100, 0), (3, 100, 0), (16, 0, 0), (1, 0, 3), (3, 100, 2)])
+def test_captured_rollout_replays_like_eager(B, K, driver):
     sh = inputs.small_shape(dtype="bf16")
     eng = make_engine(sh, max_B=B, max_K=K, dw=device_weights(cached_weights(sh, 0, _scales(sh))))
+    eng.set_driver(driver)
     r1 = inputs.make_requests(sh, list(range(500, 500 + B)))
     r2 = inputs.make_requests(sh, list(range(600, 600 + B)))
     hid, s, ver = device_requests(r1)
@@ -53,4 +56,10 @@ def test_captured_rollout_replays_like_eager(B, K):
     torch.cuda.synchronize()
     assert eng.status() == 0
     np.testing.assert_array_equal(out.cpu().numpy(), eager2.cpu().numpy())
+    for _ in range(3):  # repeated replays of the same inputs
+        out.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert eng.status() == 0
+        np.testing.assert_array_equal(out.cpu().numpy(), eager2.cpu().numpy())
     eng.close()

@@ -24,11 +24,14 @@ def _scales(sh):
     return (("emb", 1.0), ("w_ih", sh.E ** -0.5), ("w_hh", sh.G ** -0.5), ("fc1", 0.5 * sh.G ** -0.5), ("fc2", 0.2))
 
 
-# barrier 1 follows the seed update, 3 the first projector phase, 4 the
-# first correction phase
+# grid-barrier kernel: barrier 1 follows the seed update, 3 the first
+# projector phase, 4 the first correction phase; tagged-exchange kernel:
+# publication 1 is the seed's hidden-side products, 3 those of update 2,
+# 4 the first step's best
+@pytest.mark.parametrize("driver", [2, 3], ids=["tagged", "grid"])
 @pytest.mark.parametrize("barrier", [1, 3, 4])
 @pytest.mark.parametrize("B,K", [(1, 0), (3, 100)])
-def test_withheld_barrier_arrival_times_out_and_recovers(barrier, B, K):
+def test_withheld_barrier_arrival_times_out_and_recovers(barrier, B, K, driver):
     from speculative_decoding_draft_lm_gb300 import rollout as R
     sh = inputs.small_shape(dtype="bf16")
     sc = _scales(sh)
@@ -37,7 +40,7 @@ def test_withheld_barrier_arrival_times_out_and_recovers(barrier, B, K):
     r = inputs.make_requests(sh, list(range(70, 70 + B)))
     o = oracle.rollout(ow, r["hidden"], r["s"], r["verified"], K)
     eng = make_engine(sh, max_B=B, max_K=K, dw=device_weights(w))
-    eng.set_driver(R.DOMINO_DRIVER_PERSISTENT)
+    eng.set_driver(driver)
     dreq = device_requests(r)
     eng.run(*dreq, K=K)  # an ordinary run first
     assert eng.status() == R.DOMINO_OK
