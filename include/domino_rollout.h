@@ -226,9 +226,9 @@ DOMINO_API int domino_rollout_status(domino_ctx* ctx, void* cuda_stream);
  * withhold its n-th synchronisation: its arrival at the n-th grid barrier
  * (barriers 1 and 2 follow the two seed updates; each corrected step then
  * has two, or three for more than four requests), or in the tagged-exchange
- * driver its n-th publication (1: the seed's hidden-side products; then per
- * step its activations, its hidden-side products of the next update unless
- * the step is the last, and its best).  Nothing replaces it, so the bounded
+ * driver its n-th publication (1: its GRU units after the seed update; then
+ * per step its activations, its best, and, unless the step is the last, its
+ * GRU units after the next update).  Nothing replaces it, so the bounded
  * wait of every CTA for it runs out after 200 ms, the kernel returns, the
  * run's tokens are meaningless and
  * domino_rollout_status() reports DOMINO_ERR_TIMEOUT.  Nothing faults or

@@ -233,7 +233,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oC = take(g.max_K > 0 ? (size_t)g.max_B * DOMINO_MAX_VOCAB_PARTITIONS * g.max_K * 4 : 0);
     const bool ll = g.dtype == DOMINO_DTYPE_BF16;  // tagged-exchange persistent driver
     size_t oXa = take(ll ? (size_t)2 * kLLMaxBatch * g.F * 8 : 0);
-    size_t oXg = take(ll ? (size_t)2 * kLLMaxBatch * 3 * g.G * 8 : 0);
+    size_t oXg = take(ll ? (size_t)2 * kLLMaxBatch * g.G * 8 : 0);
     size_t oXb = take(ll ? (size_t)2 * c->num_sms * kLLMaxBatch * 8 : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
@@ -260,7 +260,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->pmask = pmask ? (uint32_t*)(base + oM) : nullptr;
     c->cand = g.max_K > 0 ? (int32_t*)(base + oC) : nullptr;
     c->xa = ll ? (unsigned long long*)(base + oXa) : nullptr;
-    c->xgh = ll ? (unsigned long long*)(base + oXg) : nullptr;
+    c->xh = ll ? (unsigned long long*)(base + oXg) : nullptr;
     c->xbest = ll ? (unsigned long long*)(base + oXb) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||

@@ -181,7 +181,7 @@ struct domino_ctx {
     int* err;                 // device error word
     unsigned int* sync;       // grid-barrier words, per-step claim counters and the run counter
     unsigned long long* xa;     // [2][kLLMaxBatch,F] tagged activations (tagged-exchange driver)
-    unsigned long long* xgh;    // [2][kLLMaxBatch,3G] tagged hidden-side products
+    unsigned long long* xh;     // [2][kLLMaxBatch,G] tagged GRU state
     unsigned long long* xbest;  // [2][num_sms,kLLMaxBatch] per-CTA best of a step
     float* gi_table;          // [V, 3G] input-side GRU pre-activations of every token (built at load)
     float* gh_next;           // [kPersistGruGroup][3G] hidden-side pre-activations of the next GRU update (persistent driver)

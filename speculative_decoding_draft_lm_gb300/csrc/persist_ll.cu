@@ -3,18 +3,18 @@
 //
 // Per corrected step k (page "Add correctness-first Domino support to DFlash
 // V2", section "Design"; page "[Spec] Add Domino projector support to DFlash
-// speculative decoding (V2)", section "Implementation"):
-//   P_k  every CTA holds the whole state h_k in shared memory; it computes its
-//        slice of a = SiLU(fc1 h_k + s[k]) and publishes it, then its units'
-//        hidden-side products W_hh h_k of the next GRU update, and publishes
-//        them too;
-//   C_k  every CTA reads all of a, scores its slice of fc2 rows (full
-//        vocabulary, B = 1) or of the pool entries,
-//        c[v] = fc2[v].a + bias[v] + L[b,k+1,v], and publishes its best
-//        (value, id) per request;
-//   then every CTA reads all the bests, takes p_{k+1} (lowest id on ties),
-//   and rebuilds h_{k+1} = GRU(emb[p_{k+1}], h_k) for all units from the
-//   token-table row and the published hidden-side products.
+// speculative decoding (V2)", section "Implementation"), every CTA holds the
+// whole GRU state h_k in shared memory and
+//   P_k  computes its slice of a = SiLU(fc1 h_k + s[k]) and publishes it, and
+//        the hidden-side products W_hh h_k of its own GRU units (kept);
+//   C_k  reads all of a, scores its slice of fc2 rows (full vocabulary,
+//        B = 1) or of the pool entries, c[v] = fc2[v].a + bias[v] +
+//        L[b,k+1,v], and publishes its best (value, id) per request;
+//   X_k  reads every CTA's best, takes p_{k+1} (lowest id on ties), updates
+//        its own units, h_{k+1}[j] = GRU(emb[p_{k+1}], h_k)[j], from the
+//        token-table row's three entries and its kept products, and
+//        publishes them;
+//   H_k  reads the whole new state.
 //
 // Exchange words are 64 bits: a 32-bit payload with a 32-bit tag (run epoch
 // * 16 + step), or for the per-CTA bests the packed key (orderable value, low
@@ -22,20 +22,22 @@
 // and tag together, and a reader polls the word until its tag is the one it
 // waits for, so a read of the data is also the synchronisation (no separate
 // barrier round trip).  Each word has one writer per step.  Every exchange
-// is double-buffered by step parity: a CTA that publishes nothing another one
+// is double-buffered by step parity: a CTA that publishes nothing another
 // waits for (e.g. one without projector rows) may still be reading step k's
 // words when a faster CTA publishes step k+1, but no CTA can publish step
 // k+2 before every CTA has published something that follows its reading of
-// step k (its best of step k or k+1), so a buffer is never overwritten while
-// it is read.
+// step k, so a buffer is never overwritten while it is read.
 //
-// The W_hh rows of a CTA's units and its fc1 rows stay in shared memory for
-// the whole launch; pool rows too, when they fit.  Over the full vocabulary a
-// producer warp streams fc2 with bulk copies into a ring (walking the slice
-// in alternating directions so a step starts on the rows the last one read);
-// the last seventh of every slice is shared: producers that finish their own
-// part early claim those chunks through a per-step counter, which absorbs the
-// per-step spread of the CTAs' streaming rates.
+// Dot products use a lane layout without shared-memory bank conflicts: lane
+// l holds elements 128c + 4l .. 128c + 4l + 3 of a row or vector.  A warp
+// keeps up to two weight rows in registers and streams the state through
+// 16-byte shared loads.  The fc1 rows of a CTA, and for pools its W_hh rows
+// and pool rows, stay in shared memory for the whole launch.  Over the full
+// vocabulary a producer warp streams fc2 with bulk copies into a ring
+// (walking the slice in alternating directions so a step starts on the rows
+// the last one read); the last seventh of every slice is shared: producers
+// that finish their own part early claim those chunks through a per-step
+// counter, which absorbs the per-step spread of the CTAs' streaming rates.
 //
 // Every wait (exchange word, ring slot) is bounded; on a timeout the kernel
 // raises the device error word, and all consumer warps leave together (the
@@ -49,9 +51,9 @@ using namespace persist;
 
 namespace {
 
-constexpr int kRows = 4;        // fc2 rows per ring slot
+constexpr int kRows = 4;           // fc2 rows per ring slot
 constexpr int kMaxSlots = 64;
-constexpr int kShareDiv = 7;    // a seventh of each full-vocabulary slice is shared
+constexpr int kShareDiv = 7;       // a seventh of each full-vocabulary slice is shared
 constexpr int kProducerLanes = 4;  // lanes of the producer warp that issue copies
 constexpr int kMaxSeg = 2048;
 constexpr unsigned kBestTagMask = 0x3FFFu;  // low 14 bits of a best word: the step
@@ -66,9 +68,9 @@ struct LLParams {
     int *bad, *err;
     unsigned* claim;        // [16] per-step shared-chunk counters, zeroed per run
     const unsigned* epoch;  // run counter, bumped per run before this kernel
-    unsigned long long* xa;     // [2][kLLMaxBatch][F]   by step parity
-    unsigned long long* xgh;    // [2][kLLMaxBatch][3G]  by update parity
-    unsigned long long* xbest;  // [2][grid][kLLMaxBatch] by step parity, zeroed per run
+    unsigned long long* xa;     // [2][kLLMaxBatch][F]   activations, by step parity
+    unsigned long long* xh;     // [2][kLLMaxBatch][G]   GRU state, by update parity
+    unsigned long long* xbest;  // [2][grid][kLLMaxBatch] per-CTA bests, by step parity, zeroed per run
     float *dbg_h, *dbg_z, *dbg_scores;
     unsigned long long* trace;
     int B, K, V, G, F;
@@ -81,7 +83,7 @@ struct LLParams {
 };
 
 struct LLLayout {
-    int ring, bars, srow, swhh, sfc1, sh, sa, sL, sbias, stot, spid, ss, sgh0, sred, stok, misc, total;
+    int ring, bars, srow, swhh, sfc1, sh, sa, sL, sbias, spid, ss, sgh, sred, stok, misc, total;
     __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B,
                                  bool wh_res) {
         auto up = [](int x) { return (x + 127) & ~127; };
@@ -95,11 +97,10 @@ struct LLLayout {
         sa = o;    o = up(o + 4 * B * F);
         sL = o;    o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
-        stot = o;  o = up(o + 4 * seg);
-        spid = o;  o = up(o + 4 * seg);                        // pool ids of the slice
-        ss = o;    o = up(o + 4 * B * kProposals * fpc);       // s rows of the CTA's projector outputs
-        sgh0 = o;  o = up(o + 4 * B * 3 * jpc);
-        sred = o;  o = up(o + 8 * (kConsumerWarps + 1) * kLLMaxBatch);
+        spid = o;  o = up(o + 4 * seg);                   // pool ids of the slice
+        ss = o;    o = up(o + 4 * B * kProposals * fpc);  // s entries of the CTA's projector outputs
+        sgh = o;   o = up(o + 4 * B * 3 * jpc);           // hidden-side products of the CTA's units
+        sred = o;  o = up(o + 8 * 2 * kLLMaxBatch);
         stok = o;  o = up(o + 4 * kLLMaxBatch);
         misc = o;  o = up(o + 64);
         total = o;
@@ -118,56 +119,97 @@ __device__ __forceinline__ unsigned long long tagged(float x, unsigned tag) {
     return ((unsigned long long)tag << 32) | __float_as_uint(x);
 }
 
-// Spin until the word at p satisfies `ok` (its tag has arrived); bounded.
-// Returns the word; on a timeout (or when another thread of the CTA gave up)
-// sets *failed.
-template <typename Ok>
-__device__ __forceinline__ unsigned long long poll_word(const unsigned long long* p, unsigned long long v, Ok ok,
-                                                        volatile int* abort_flag, int* err, bool& failed) {
-    if (ok(v)) return v;
+// Does word w carry `tag`?  Mode 0: in its high 32 bits (tagged payloads);
+// mode 1: in its low 14 bits (per-CTA bests).
+__device__ __forceinline__ bool has_tag(unsigned long long w, unsigned tag, int mode) {
+    return mode == 0 ? (unsigned)(w >> 32) == tag : (unsigned)(w & kBestTagMask) == tag;
+}
+
+// Spin until the word at p carries `tag`; bounded.  Returns the last word
+// read: without the tag on a timeout (which also raises the CTA's abort flag
+// and the device error word) or when another thread of the CTA gave up.
+// Out of line: the common case (the word has arrived) never calls it.
+__device__ __noinline__ unsigned long long poll_slow(const unsigned long long* p, unsigned tag, int mode,
+                                                     volatile int* abort_flag, int* err) {
     const unsigned long long t0 = tc::globaltimer();
+    unsigned long long v;
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i) {
+            __nanosleep(64);  // every spinning thread of every CTA polls L2: keep its request rate down
             v = ld_relaxed_u64(p);
-            if (ok(v)) return v;
+            if (has_tag(v, tag, mode)) return v;
         }
-        if (*abort_flag) {
-            failed = true;
-            return v;
-        }
+        if (*abort_flag) return v;
         if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
             *abort_flag = 1;
             atomicOr(err, kErrTimeout);
-            failed = true;
             return v;
         }
     }
 }
 
-// dot of a bf16 shared-memory row with an fp32 shared-memory vector, lane
-// partial (lane l covers elements (l + 32c)*8 .. +7)
-template <int NCH>
-__device__ __forceinline__ float smem_dot(const __nv_bfloat16* row, const float* x, int n, int lane) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int e = (lane + 32 * c) * 8;
-        if (e < n) {
-            float w[8], v[8];
-            lds8(row + e, w);
-            lds8(x + e, v);
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                a0 = fmaf(w[i], v[i], a0);
-                a1 = fmaf(w[i + 1], v[i + 1], a1);
-            }
-        }
-    }
-    return a0 + a1;
+// The word at p with `tag`, given a first read v; sets `failed` if it never came.
+__device__ __forceinline__ unsigned long long poll_word(const unsigned long long* p, unsigned long long v,
+                                                        unsigned tag, int mode, volatile int* abort_flag, int* err,
+                                                        bool& failed) {
+    if (has_tag(v, tag, mode)) return v;
+    v = poll_slow(p, tag, mode, abort_flag, err);
+    if (!has_tag(v, tag, mode)) failed = true;
+    return v;
 }
 
-template <int NCH>
+// A bf16 row in the conflict-free lane layout: lane l holds elements
+// 128c + 4l .. +3 (c < NC) as two packed bf16 pairs.
+template <int NC>
+struct Row4 {
+    uint2 q[NC];
+    __device__ __forceinline__ void load_smem(const __nv_bfloat16* row, int n, int lane) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int e = c * 128 + 4 * lane;
+            q[c] = e < n ? *reinterpret_cast<const uint2*>(row + e) : make_uint2(0u, 0u);
+        }
+    }
+    __device__ __forceinline__ void load_global(const __nv_bfloat16* row, int n, int lane, uint64_t pol) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int e = c * 128 + 4 * lane;
+            if (e < n)
+                asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                             : "=r"(q[c].x), "=r"(q[c].y)
+                             : "l"(row + e), "l"(pol));
+            else
+                q[c] = make_uint2(0u, 0u);
+        }
+    }
+};
+
+// fp32 shared-memory vector chunk c of this lane (zero past n)
+__device__ __forceinline__ float4 vec4(const float* x, int c, int n, int lane) {
+    const int e = c * 128 + 4 * lane;
+    return e < n ? *reinterpret_cast<const float4*>(x + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ void fma4(uint2 w, float4 x, float& a0, float& a1) {
+    float w0, w1, w2, w3;
+    bf16x2_to_f32(w.x, w0, w1);
+    bf16x2_to_f32(w.y, w2, w3);
+    a0 = fmaf(w0, x.x, a0);
+    a1 = fmaf(w1, x.y, a1);
+    a0 = fmaf(w2, x.z, a0);
+    a1 = fmaf(w3, x.w, a1);
+}
+
+// Two warp sums at once (their shuffles interleaved).
+__device__ __forceinline__ void warp_sum2(float& a, float& b) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+}
+
+template <int NC>
 __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     extern __shared__ __align__(128) uint8_t sm[];
     const int B = p.B, V = p.V, G = p.G, F = p.F;
@@ -183,10 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     float* sa = reinterpret_cast<float*>(sm + lay.sa);
     float* sL = reinterpret_cast<float*>(sm + lay.sL);
     float* sbias = reinterpret_cast<float*>(sm + lay.sbias);
-    float* stot = reinterpret_cast<float*>(sm + lay.stot);
     int* spid = reinterpret_cast<int*>(sm + lay.spid);
     float* ss = reinterpret_cast<float*>(sm + lay.ss);
-    float* sgh0 = reinterpret_cast<float*>(sm + lay.sgh0);
+    float* sgh = reinterpret_cast<float*>(sm + lay.sgh);
     unsigned long long* sred = reinterpret_cast<unsigned long long*>(sm + lay.sred);
     int* stok = reinterpret_cast<int*>(sm + lay.stok);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + lay.misc);
@@ -324,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     // ------------------------------------------------------------------ consumers
     bool failed = false;
     const uint64_t pol_keep = tc::policy_evict_last();
-    // resident weights: this CTA's W_hh rows (3 gates x its units) and fc1 rows
+    // resident weights: this CTA's fc1 rows and (pools) its units' W_hh rows
     {
         const int per_row = G / 8;  // 16-byte pieces of a row
         for (int i = tid; i < (p.wh_res ? 3 * jn * per_row : 0); i += kConsumerWarps * 32) {
@@ -341,19 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     }
     if (full_vocab)
         for (int i = tid; i < nw; i += kConsumerWarps * 32) sbias[i] = __bfloat162float(p.bias[w0 + i]);
-
-    // W_hh row `gate*G + j0 + jj` dotted with the state of every request:
-    // from shared memory, or with the row held in registers from L2
-    auto whh_dots = [&](int gate, int jj, float* out) {
-        if (p.wh_res) {
-            const __nv_bfloat16* row = swhh + ((size_t)gate * p.jpc + jj) * G;
-            for (int b = 0; b < B; ++b) out[b] = warp_sum(smem_dot<NCH>(row, sh + b * G, G, lane));
-        } else {
-            RegRow<__nv_bfloat16, NCH> w;
-            w.load(p.w_hh + ((size_t)gate * G + j0 + jj) * G, G, lane, pol_keep);
-            for (int b = 0; b < B; ++b) out[b] = warp_sum(row_dot_smem(w, sh + b * G, G, lane));
-        }
-    };
 
     // trace stamps (thread 0): slot s = time at the end of phase s
     unsigned long long* tr = p.trace ? p.trace + (size_t)cta * DOMINO_TRACE_SLOTS : nullptr;
@@ -375,6 +403,98 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             t = 0;
         }
         return t;
+    };
+
+    // ---- projector items of this CTA: its fc1 rows (item < fn, k > 0) and
+    // its units' W_hh rows (item >= fn, when gh is set).  A warp takes two
+    // items at a time with their rows in registers and streams each
+    // request's state from shared memory once for both.
+    auto project = [&](int k, bool gh, bool pub_a, unsigned tag_a, unsigned long long* xa_k) {
+        const int nf = k > 0 ? fn : 0;
+        const int n_items = nf + (gh ? 3 * jn : 0);
+        auto load = [&](int it, Row4<NC>& r) {
+            if (it < nf) {
+                r.load_smem(sfc1 + (size_t)it * G, G, lane);
+            } else {
+                const int g = it - nf, gate = g / jn, jj = g % jn;
+                if (p.wh_res) r.load_smem(swhh + ((size_t)gate * p.jpc + jj) * G, G, lane);
+                else r.load_global(p.w_hh + ((size_t)gate * G + j0 + jj) * G, G, lane, pol_keep);
+            }
+        };
+        auto finish = [&](int it, int b, float v) {
+            if (it < nf) {
+                const int f = f0 + it;
+                const float z = v + ss[(b * kProposals + k) * p.fpc + it];
+                if (pub_a) st_relaxed_u64(xa_k + (size_t)b * F + f, tagged(z * sigmoidf_(z), tag_a));
+                if (p.dbg_z) p.dbg_z[((size_t)b * kCorrected + (k - 1)) * F + f] = z;
+            } else {
+                const int g = it - nf, gate = g / jn, jj = g % jn;
+                sgh[(b * 3 + gate) * p.jpc + jj] = v;
+            }
+        };
+        // fc1 items first (the activations are on the critical path), then
+        // the W_hh items; a warp pairs items of the same kind
+        auto run = [&](int lo, int hi) {
+            for (int it0 = lo + warp; it0 < hi; it0 += 2 * kConsumerWarps) {
+                const int it1 = it0 + kConsumerWarps;
+                const bool two = it1 < hi;
+                Row4<NC> r0, r1;
+                load(it0, r0);
+                if (two) load(it1, r1);
+                for (int b = 0; b < B; ++b) {
+                    float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const float4 x = vec4(sh + b * G, c, G, lane);
+                        fma4(r0.q[c], x, a0, a1);
+                        if (two) fma4(r1.q[c], x, c0, c1);
+                    }
+                    float d0 = a0 + a1, d1 = c0 + c1;
+                    warp_sum2(d0, d1);
+                    if (lane == 0) {
+                        finish(it0, b, d0);
+                        if (two) finish(it1, b, d1);
+                    }
+                }
+            }
+        };
+        run(0, nf);
+        run(nf, n_items);
+    };
+
+    // ---- update u of this CTA's units: h[j] = GRU(token-table row, kept
+    // hidden-side products, h_prev[j]) for j in [j0, j0+jn); published
+    auto update_own = [&](int u, bool pub, unsigned tag, unsigned long long* xh_u) {
+        for (int i = tid; i < B * jn; i += kConsumerWarps * 32) {
+            const int b = i / jn, jj = i % jn, j = j0 + jj;
+            const float* gi = p.gi_table + (size_t)stok[b] * 3 * G + j;
+            const float gr = __ldg(gi), gz = __ldg(gi + G), gn = __ldg(gi + 2 * G);
+            const float* gh = sgh + b * 3 * p.jpc + jj;
+            const float r = sigmoidf_(gr + gh[0]);
+            const float zg = sigmoidf_(gz + gh[p.jpc]);
+            const float n = tanhf(gn + r * gh[2 * p.jpc]);
+            const float h = (1.f - zg) * n + zg * sh[b * G + j];
+            if (pub) st_relaxed_u64(xh_u + (size_t)b * G + j, tagged(h, tag));
+            if (p.dbg_h) p.dbg_h[((size_t)b * kProposals + u) * G + j] = h;
+        }
+    };
+    // ---- the whole state after update u, from every CTA's published units
+    auto read_state = [&](unsigned tag, const unsigned long long* xh_u) {
+        constexpr int kNT = kConsumerWarps * 32;
+        for (int base = 0; base < B * G; base += 4 * kNT) {
+            unsigned long long w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = base + e * kNT + tid;
+                w[e] = i < B * G ? ld_relaxed_u64(xh_u + i) : 0ull;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = base + e * kNT + tid;
+                if (i < B * G)
+                    sh[i] = __uint_as_float((unsigned)poll_word(xh_u + i, w[e], tag, 0, abort_flag, p.err, failed));
+            }
+        }
     };
 
     // ---- seed update 0 (h_{-1} = 0): the verified token only, independent
@@ -403,31 +523,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     }
     cp_async_wait_all();
     cons_sync();
-    // hidden-side products of update 1 for this CTA's units, kept until the
-    // run's tag is known
-    for (int it = warp; it < 3 * jn; it += kConsumerWarps) {
-        const int gate = it / jn, jj = it % jn;
-        float v[kLLMaxBatch];
-        whh_dots(gate, jj, v);
-        if (lane == 0)
-            for (int b = 0; b < B; ++b) sgh0[(b * 3 + gate) * p.jpc + jj] = v[b];
-    }
+    project(0, true, false, 0u, nullptr);  // hidden-side products of update 1
     stamp();  // 1
     pdl_wait();  // base logits, p_1 and the pool are ready; the run counter is bumped
     const unsigned ep16 = *p.epoch * 16u;
     int pub = 0;  // publications so far (for the timeout test hook)
+    auto publish_ok = [&]() { return !(cta == 0 && ++pub == p.drop_at); };
     // the buffers of update u / step k
-    auto xgh_of = [&](int u) { return p.xgh + (size_t)(u & 1) * kLLMaxBatch * 3 * G; };
+    auto xh_of = [&](int u) { return p.xh + (size_t)(u & 1) * kLLMaxBatch * G; };
     auto xa_of = [&](int k) { return p.xa + (size_t)(k & 1) * kLLMaxBatch * F; };
     auto xbest_of = [&](int k) { return p.xbest + (size_t)(k & 1) * grid * kLLMaxBatch; };
-    auto publish_ok = [&]() { return !(cta == 0 && ++pub == p.drop_at); };
-    cons_sync();
-    if (publish_ok())
-        for (int i = tid; i < B * 3 * jn; i += kConsumerWarps * 32) {
-            const int b = i / (3 * jn), r = i % (3 * jn), gate = r / jn, jj = r % jn;
-            st_relaxed_u64(xgh_of(1) + (size_t)b * 3 * G + gate * G + j0 + jj,
-                           tagged(sgh0[(b * 3 + gate) * p.jpc + jj], ep16 + 1));
-        }
     if (!full_vocab)
         for (int i = tid; i < nw; i += kConsumerWarps * 32) {
             const int v = p.pool[w0 + i];
@@ -441,62 +546,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         const int b = i / (kProposals * fn), r = i % (kProposals * fn), j = r / fn, f = r % fn;
         ss[(b * kProposals + j) * p.fpc + f] = __bfloat162float(p.s[((size_t)b * kProposals + j) * F + f0 + f]);
     }
-
-    // ---- GRU update u: every CTA rebuilds the whole state in sh from the
-    // token-table row of the fed token and the published hidden-side products
-    auto gru_update = [&](int u) {
-        const unsigned tag = ep16 + (unsigned)u;
-        constexpr int kPer = 3;
-        constexpr int kNT = kConsumerWarps * 32;
-        for (int base = 0; base < B * G; base += kPer * kNT) {
-            float gi[kPer][3];
-            unsigned long long gh[kPer][3];
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) {  // every load of the round before any use
-                const int i = base + e * kNT + tid;
-                if (i < B * G) {
-                    const int b = i / G, j = i % G;
-                    const float* g = p.gi_table + (size_t)stok[b] * 3 * G + j;
-                    const unsigned long long* x = xgh_of(u) + (size_t)b * 3 * G + j;
-#pragma unroll
-                    for (int q = 0; q < 3; ++q) {
-                        gi[e][q] = __ldg(g + q * G);
-                        gh[e][q] = ld_relaxed_u64(x + q * G);
-                    }
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) {
-                const int i = base + e * kNT + tid;
-                if (i < B * G) {
-                    const int b = i / G, j = i % G;
-                    const unsigned long long* x = xgh_of(u) + (size_t)b * 3 * G + j;
-                    float hv[3];
-#pragma unroll
-                    for (int q = 0; q < 3; ++q) {
-                        const unsigned long long w = poll_word(
-                            x + q * G, gh[e][q], [&](unsigned long long v) { return (unsigned)(v >> 32) == tag; },
-                            abort_flag, p.err, failed);
-                        hv[q] = __uint_as_float((unsigned)w);
-                    }
-                    const float r = sigmoidf_(gi[e][0] + hv[0]);
-                    const float zg = sigmoidf_(gi[e][1] + hv[1]);
-                    const float n = tanhf(gi[e][2] + r * hv[2]);
-                    const float h = (1.f - zg) * n + zg * sh[b * G + j];
-                    sh[b * G + j] = h;
-                    if (p.dbg_h && j >= j0 && j < j0 + jn) p.dbg_h[((size_t)b * kProposals + u) * G + j] = h;
-                }
-            }
-        }
-    };
-
     // update 1 consumes p_1 (the LM-head's argmax of base row 1)
     if (tid < B) stok[tid] = fed_token(tid, 1, (int)key_index(__ldcg(&p.keys[(size_t)tid * kBlock])));
+    // per-request best of this CTA's rows (sbest_c) and of every CTA's bests
+    // (sbest_x), folded with shared-memory atomics; cleared after each read
+    unsigned long long* sbest_c = sred;
+    unsigned long long* sbest_x = sred + kLLMaxBatch;
+    if (tid < 2 * kLLMaxBatch) sred[tid] = 0ull;
     cons_sync();
-    gru_update(1);
+    update_own(1, publish_ok(), ep16 + 1, xh_of(1));
+    cons_sync();  // every read of the old state is done
+    read_state(ep16 + 1, xh_of(1));
     if (cons_sync_or(failed)) return;
     stamp();  // 2
 
+    // correction: lane l holds elements (l + 32c)*8 .. +7 of a row (16-byte
+    // shared loads of the ring's rows); the activations of one request in registers
+    constexpr int NCH = (NC + 1) / 2;  // 256-element chunks
     float areg[NCH][8];
     int areg_b = -1;
     auto load_areg = [&](int b) {
@@ -568,20 +634,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         return ((unsigned long long)ord_f32(c) << 32) |
                ((unsigned long long)(~(uint32_t)v & 0x3FFFFu) << kBestIdShift);
     };
-    // per-request maxima of this thread's m[] over the CTA into sred[15*kLLMaxBatch + b]
-    auto block_max = [&](unsigned long long* m) {
-        for (int b = 0; b < B; ++b) {
-            const unsigned long long w = warp_max_u64(m[b]);
-            if (lane == 0) sred[warp * kLLMaxBatch + b] = w;
-        }
-        cons_sync();
-        if (tid < B) {
-            unsigned long long w = 0ull;
-            for (int i = 0; i < kConsumerWarps; ++i) w = max(w, sred[i * kLLMaxBatch + tid]);
-            sred[kConsumerWarps * kLLMaxBatch + tid] = w;
-        }
-        cons_sync();
-    };
 
     const int rsel = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);  // the slot row this lane finishes
     int qw = warp;  // ring: sequence number of this warp's next slot (slot q is consumed by warp q % n_cons)
@@ -600,35 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         }
         cp_async_commit();
 
-        // ---- P_k: the projector slice (published first), then the next
-        // update's hidden-side products of this CTA's units
-        {
-            const bool pub_a = publish_ok();
-            const bool pub_g = k < p.n_corr && publish_ok();
-            const int n_items = fn + (k < p.n_corr ? 3 * jn : 0);
-            for (int it = warp; it < n_items; it += kConsumerWarps) {
-                if (it < fn) {
-                    const __nv_bfloat16* row = sfc1 + (size_t)it * G;
-                    for (int b = 0; b < B; ++b) {
-                        const float v = warp_sum(smem_dot<NCH>(row, sh + b * G, G, lane));
-                        if (lane == 0) {
-                            const int f = f0 + it;
-                            const float z = v + ss[(b * kProposals + k) * p.fpc + it];
-                            if (pub_a) st_relaxed_u64(xa_of(k) + (size_t)b * F + f, tagged(z * sigmoidf_(z), tag_k));
-                            if (p.dbg_z) p.dbg_z[((size_t)b * kCorrected + (k - 1)) * F + f] = z;
-                        }
-                    }
-                } else {
-                    const int g = it - fn, gate = g / jn, jj = g % jn;
-                    float v[kLLMaxBatch];
-                    whh_dots(gate, jj, v);
-                    if (lane == 0 && pub_g)
-                        for (int b = 0; b < B; ++b)
-                            st_relaxed_u64(xgh_of(k + 1) + (size_t)b * 3 * G + gate * G + j0 + jj,
-                                           tagged(v[b], ep16 + (unsigned)(k + 1)));
-                }
-            }
-        }
+        // ---- P_k: the projector slice (published), and the next update's
+        // hidden-side products of this CTA's units (kept)
+        project(k, k < p.n_corr, publish_ok(), tag_k, xa_of(k));
         stamp();  // 3 + 4(k-1): projector published
         // ---- C_k: all activations, then this CTA's slice
         {
@@ -645,9 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 for (int e = 0; e < 4; ++e) {
                     const int i = base + e * kNT + tid;
                     if (i < B * F)
-                        sa[i] = __uint_as_float((unsigned)poll_word(
-                            xa + i, w[e], [&](unsigned long long v) { return (unsigned)(v >> 32) == tag_k; },
-                            abort_flag, p.err, failed));
+                        sa[i] = __uint_as_float((unsigned)poll_word(xa + i, w[e], tag_k, 0, abort_flag, p.err, failed));
                 }
             }
         }
@@ -655,36 +679,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         if (cons_sync_or(failed)) return;
         areg_b = -1;
         stamp();  // 4 + 4(k-1): activations in
-        unsigned long long best_direct = 0ull;  // shared rows finished in the slot loop (full vocabulary)
-        if (p.resident) {
-            for (int c = warp; c < n_chunks; c += kConsumerWarps) {
-                if (k == 1 && !tc::mbar_wait(full0 + 8 * c, 0u, abort_flag, p.err)) {
-                    failed = true;
-                    break;
+        unsigned long long m[kLLMaxBatch];  // this lane's best per request of the rows it finishes
+#pragma unroll
+        for (int b = 0; b < kLLMaxBatch; ++b) m[b] = 0ull;
+        // one loop for both layouts (a single copy of the slot code): resident
+        // pool rows, chunk c in slot c; or ring slots, slot q for warp q % n_cons
+        {
+            int c_res = warp;
+            const bool active = p.resident ? true : warp < p.n_cons;
+            while (active) {
+                int slot;
+                long long item0;
+                if (p.resident) {
+                    if (c_res >= n_chunks) break;
+                    slot = c_res;
+                    c_res += kConsumerWarps;
+                    if (k == 1 && !tc::mbar_wait(full0 + 8 * slot, 0u, abort_flag, p.err)) {
+                        failed = true;
+                        break;
+                    }
+                    item0 = w0 + slot * kRows;
+                } else {
+                    const int q = qw;
+                    qw += p.n_cons;
+                    slot = q % p.n_slots;
+                    if (!tc::mbar_wait(full0 + 8 * slot, (uint32_t)((q / p.n_slots) & 1), abort_flag, p.err)) {
+                        failed = true;
+                        break;
+                    }
+                    item0 = srow[slot];
+                    if (item0 < 0) {  // end of this step for this warp
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
+                        break;
+                    }
                 }
-                const int nr = min(kRows, nw - c * kRows);
-                float part[kRows];
-                slot_dots(reinterpret_cast<const __nv_bfloat16*>(ring + (size_t)c * slot_bytes), w0 + c * kRows, nr,
-                          part);
-                const float tot = warp_sum4(part[0], part[1], part[2], part[3], lane);
-                if ((lane & 7) == 0 && rsel < nr) stot[c * kRows + rsel] = tot;
-            }
-        } else if (warp < p.n_cons) {
-            while (true) {
-                const int q = qw;
-                qw += p.n_cons;
-                const int slot = q % p.n_slots;
-                if (!tc::mbar_wait(full0 + 8 * slot, (uint32_t)((q / p.n_slots) & 1), abort_flag, p.err)) {
-                    failed = true;
-                    break;
-                }
-                const int item0 = srow[slot];
-                if (item0 < 0) {  // end of this step for this warp
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);
-                    break;
-                }
-                const int nr = full_vocab ? min(kRows, V - item0) : min(kRows, (int)(w1 - item0));
+                const int nr = full_vocab ? min(kRows, V - (int)item0) : min(kRows, (int)(w1 - item0));
                 const bool own = item0 >= w0 + st_lo && item0 < w0 + st_hi;
                 // a shared row: this lane fetches its bias and base logit before the dots
                 float tail = 0.f;
@@ -693,68 +723,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                            __ldg(p.L + (size_t)(kRowOffset + k) * V + item0 + rsel);
                 float part[kRows];
                 slot_dots(reinterpret_cast<const __nv_bfloat16*>(ring + (size_t)slot * slot_bytes), item0, nr, part);
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);  // the slot is read
+                if (!p.resident) {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(empty0 + 8 * slot);  // the slot is read
+                }
                 const float tot = warp_sum4(part[0], part[1], part[2], part[3], lane);
                 if ((lane & 7) == 0 && rsel < nr) {
-                    if (own) {
-                        stot[item0 - w0 + rsel] = tot;
-                    } else {
-                        const float cv = tot + tail;
-                        best_direct = max(best_direct, best_key(cv, item0 + rsel));
-                        if (p.dbg_scores) p.dbg_scores[(size_t)(k - 1) * V + item0 + rsel] = cv;
+                    // finish the row: bias and base logit (own rows: staged; shared rows: fetched above)
+                    const int item = (int)item0 + rsel, r = item - (int)w0;
+                    const int b = full_vocab ? 0 : item / p.K;
+                    const int v = full_vocab ? item : spid[r];
+                    const float cv = own ? tot + sbias[r] + sL[r] : tot + tail;
+                    const unsigned long long key = best_key(cv, v);
+#pragma unroll
+                    for (int bb = 0; bb < kLLMaxBatch; ++bb)
+                        if (bb == b) m[bb] = max(m[bb], key);
+                    if (p.dbg_scores) {
+                        if (full_vocab) p.dbg_scores[(size_t)(k - 1) * V + v] = cv;
+                        else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + item % p.K] = cv;
                     }
                 }
             }
         }
+        for (int b = 0; b < B; ++b) {
+            const unsigned long long w = warp_max_u64(m[b]);
+            if (lane == 0 && w) atomicMax(&sbest_c[b], w);
+        }
         if (cons_sync_or(failed)) return;
-        // ---- finish this CTA's rows: bias, base logit, per-request best
         {
-            unsigned long long m[kLLMaxBatch];
-#pragma unroll
-            for (int b = 0; b < kLLMaxBatch; ++b) m[b] = 0ull;
-            m[0] = best_direct;
-            for (int r = st_lo + tid; r < st_hi; r += kConsumerWarps * 32) {
-                const long long item = w0 + r;
-                const int b = full_vocab ? 0 : (int)(item / p.K);
-                const int v = full_vocab ? (int)item : spid[r];
-                const float cv = stot[r] + sbias[r] + sL[r];
-                const unsigned long long key = best_key(cv, v);
-#pragma unroll
-                for (int bb = 0; bb < kLLMaxBatch; ++bb)
-                    if (bb == b) m[bb] = max(m[bb], key);
-                if (p.dbg_scores) {
-                    if (full_vocab) p.dbg_scores[(size_t)(k - 1) * V + v] = cv;
-                    else p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + (int)(item % p.K)] = cv;
-                }
-            }
-            block_max(m);
             const bool pub_b = publish_ok();
-            if (tid < B && pub_b)
-                st_relaxed_u64(xbest_of(k) + (size_t)cta * kLLMaxBatch + tid,
-                               sred[kConsumerWarps * kLLMaxBatch + tid] | (unsigned long long)k);
+            if (tid < B) {
+                if (pub_b)
+                    st_relaxed_u64(xbest_of(k) + (size_t)cta * kLLMaxBatch + tid, sbest_c[tid] | (unsigned long long)k);
+                sbest_c[tid] = 0ull;
+            }
         }
         stamp();  // 5 + 4(k-1): best published
         if (k == p.n_corr && cta != 0) return;  // only CTA 0 reports the last step
-        // ---- every CTA's best of step k: p_{k+1} for every request
+        // ---- X_k: every CTA's best of step k gives p_{k+1} for every request
         {
-            unsigned long long m[kLLMaxBatch];
-#pragma unroll
-            for (int b = 0; b < kLLMaxBatch; ++b) m[b] = 0ull;
             const unsigned kk = (unsigned)k;
             for (int i = tid; i < grid * B; i += kConsumerWarps * 32) {
                 const int c = i / B, b = i % B;
                 const unsigned long long* x = xbest_of(k) + (size_t)c * kLLMaxBatch + b;
-                const unsigned long long w = poll_word(
-                    x, ld_relaxed_u64(x), [&](unsigned long long v) { return (unsigned)(v & kBestTagMask) == kk; },
-                    abort_flag, p.err, failed);
-#pragma unroll
-                for (int bb = 0; bb < kLLMaxBatch; ++bb)
-                    if (bb == b) m[bb] = max(m[bb], w & ~(unsigned long long)kBestTagMask);
+                const unsigned long long w = poll_word(x, ld_relaxed_u64(x), kk, 1, abort_flag, p.err, failed);
+                if (w > kBestTagMask) atomicMax(&sbest_x[b], w & ~(unsigned long long)kBestTagMask);
             }
-            block_max(m);
+            cons_sync();
             if (tid < B) {
-                const unsigned long long w = sred[kConsumerWarps * kLLMaxBatch + tid];
+                const unsigned long long w = sbest_x[tid];
+                sbest_x[tid] = 0ull;
                 const int id = (int)(~(uint32_t)(w >> kBestIdShift) & 0x3FFFFu);
                 if (cta == 0) p.keys[(size_t)tid * kBlock + k] = pack_key(unord_f32((uint32_t)(w >> 32)), (uint32_t)id);
                 if (k < p.n_corr) stok[tid] = fed_token(tid, k + 1, id);
@@ -762,13 +780,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         }
         if (cons_sync_or(failed)) return;
         if (k < p.n_corr) {
-            gru_update(k + 1);
+            // ---- this CTA's units of h_{k+1}, then (H_k) the whole state
+            update_own(k + 1, publish_ok(), ep16 + (unsigned)(k + 1), xh_of(k + 1));
+            cons_sync();  // every read of the old state is done
+            read_state(ep16 + (unsigned)(k + 1), xh_of(k + 1));
             if (cons_sync_or(failed)) return;
         }
         stamp();  // 6 + 4(k-1): next state built
     }
 }
-
 
 struct LLPlan {
     int seg, jpc, fpc, n_slots, n_cons, resident, wh_res, smem;
@@ -853,7 +873,7 @@ cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r) {
     p.claim = c->sync + kClaimCounters;
     p.epoch = c->sync + kRunEpochWord;
     p.xa = c->xa;
-    p.xgh = c->xgh;
+    p.xh = c->xh;
     p.xbest = c->xbest;
     p.dbg_h = r.dbg.h;
     p.dbg_z = r.dbg.z;
@@ -878,7 +898,10 @@ cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r) {
     c->drop_barrier = 0;
 
     const int mx = g.G > g.F ? g.G : g.F;
-    void (*kern)(LLParams) = mx <= 256 ? k_rollout_ll<1> : mx <= 512 ? k_rollout_ll<2> : k_rollout_ll<4>;
+    void (*kern)(LLParams) = mx <= 128   ? k_rollout_ll<1>
+                             : mx <= 256 ? k_rollout_ll<2>
+                             : mx <= 512 ? k_rollout_ll<4>
+                                         : k_rollout_ll<8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

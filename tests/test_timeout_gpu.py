@@ -26,8 +26,8 @@ def _scales(sh):
 
 # grid-barrier kernel: barrier 1 follows the seed update, 3 the first
 # projector phase, 4 the first correction phase; tagged-exchange kernel:
-# publication 1 is the seed's hidden-side products, 3 those of update 2,
-# 4 the first step's best
+# publication 1 is the CTA's GRU units after the seed, 3 the first step's
+# best, 4 its units after update 2
 @pytest.mark.parametrize("driver", [2, 3], ids=["tagged", "grid"])
 @pytest.mark.parametrize("barrier", [1, 3, 4])
 @pytest.mark.parametrize("B,K", [(1, 0), (3, 100)])
