@@ -364,9 +364,14 @@ inline int nch_of(int n) { return (n + 255) / 256; }
 template <int NCH>
 cudaError_t launch_pool_nch(domino_ctx* c, RunArgs& r, int k) {
     const domino_config& g = c->cfg;
-    // items per block: enough for 4 rows per warp and at most 64 requests a block
+    // items per block: about four blocks per SM (every warp's gathered rows in
+    // flight at once), whole 4-row groups per warp, at most 8 groups per warp
+    // and at most 64 requests a block
     long long items = (long long)r.B * r.K;
-    int ipb = 8 * kPoolRows * 8;  // 8 groups per warp
+    const int group = (kBatchThreads / 32) * kPoolRows;  // one 4-row group per warp
+    long long want = (items + 4LL * c->num_sms - 1) / (4LL * c->num_sms);
+    want = (want + group - 1) / group * group;
+    int ipb = (int)(want < group ? group : want > 8 * group ? 8 * group : want);
     if ((long long)ipb > 62LL * r.K) ipb = (int)(62LL * r.K);
     if (ipb < 1) ipb = 1;
     const long long blocks = (items + ipb - 1) / ipb;
