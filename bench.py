@@ -84,8 +84,23 @@ def alg_bytes(sh: inputs.Shape, B: int, K: int, n_prop: int = 15, s_in_library: 
     gru = 3 * G * G * e + B * (3 * G * 4 + G * 4 * 2)
     fc1 = F * G * e + B * (G * 4 + F * e + F * 4 * 2)
     pool = 0 if full else B * 15 * V * 4 + B * V * 4 * 5 + B * K * 4
-    # persistent driver: the GRU seed and the corrected steps in one launch
-    steps = max(2, n_prop) * gru + (n_prop - 1) * (fc1 + corr)
+    # persistent driver: the GRU seed and the corrected steps in one launch.
+    # A tensor counts once per launch when its working set over the whole
+    # rollout fits in 64 MB of L2, else once per step: W_hh and fc1 always
+    # fit; the pool's gathered rows fit for small B*K; fc2 over the full
+    # vocabulary does not.  Per-step rows (token table, base logits, state,
+    # s, activations) always count per step.
+    n_upd, n_corr = max(2, n_prop), n_prop - 1
+    l2_fit = 64 << 20
+    per_upd = B * (3 * G * 4 + G * 4 * 2)
+    per_fc1 = B * (G * 4 + F * e + F * 4 * 2)
+    if full:
+        corr_once, corr_step = 0, corr
+    else:
+        rows = B * K * (F * e + e + 4)
+        corr_once, corr_step = (rows, corr - rows) if rows <= l2_fit else (0, corr)
+    steps = (3 * G * G * e + F * G * e + corr_once + n_upd * per_upd +
+             n_corr * (per_fc1 + corr_step))
     per_block = lm + pool + steps
     return {"lmhead": lm, "correct": corr, "gru": gru, "fc1": fc1, "pool": pool, "steps": steps,
             "block": per_block, "lmhead_flop": lm_flop}
@@ -594,19 +609,21 @@ def read_traffic(kernel: str, workload: str):
     ent = t.get(workload, {}).get(kernel)
     if not ent:
         return None
-    if ent.get("source_hash") != source_hash():
+    if ent.get("source_hash") != source_hash(ent.get("files")):
         return None
     return ent.get("dram_bytes_per_launch")
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources with // comments and blank lines dropped, so
-    that a comment edit does not orphan the committed counters."""
+def source_hash(files=None) -> str:
+    """Hash of the kernel sources (all of them, or the listed files of the
+    captured kernel) with // comments and blank lines dropped, so that a
+    comment edit, or an edit of another kernel, does not orphan the committed
+    counters."""
     import hashlib
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_draft_lm_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files or os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in fh]

@@ -44,6 +44,7 @@ class Shape:
 TINY = Shape(V=4096, H=256, E=128, G=128, F=256, dtype="fp32")
 QWEN3_8B = Shape(V=151936, H=4096, E=1024, G=1024, F=1024, dtype="bf16")
 LARGE_TARGET = Shape(V=151936, H=5120, E=1536, G=1536, F=1536, dtype="bf16")
+QWEN3_8B_V80K = Shape(V=80000, H=4096, E=1024, G=1024, F=1024, dtype="bf16")
 
 
 @dataclass(frozen=True)
@@ -74,6 +75,11 @@ WORKLOADS = {
     "qwen3_8b_b64_k2048": Workload("qwen3_8b_b64_k2048", QWEN3_8B, 64, 2048, _seeds(64, 1)),
     "large_b64_k0": Workload("large_b64_k0", LARGE_TARGET, 64, 0, _seeds(64, 1)),
     "large_b64_k2048": Workload("large_b64_k2048", LARGE_TARGET, 64, 2048, _seeds(64, 1)),
+    # profiling cases: the Qwen3-8B hidden sizes with the vocabulary cut to
+    # 80,000 rows, so fc2 (164 MB) still exceeds L2 while the whole case
+    # holds about 2 GB of device memory
+    "qwen3_8b_v80k_b1_k0": Workload("qwen3_8b_v80k_b1_k0", QWEN3_8B_V80K, 1, 0, (1,)),
+    "qwen3_8b_v80k_b1_k2048": Workload("qwen3_8b_v80k_b1_k2048", QWEN3_8B_V80K, 1, 2048, (1,)),
 }
 
 WEIGHT_NAMES = ("lm_head", "emb", "w_ih", "w_hh", "fc1", "fc2", "b")
