@@ -159,56 +159,6 @@ __device__ __forceinline__ unsigned long long poll_word(const unsigned long long
     return v;
 }
 
-// A bf16 row in the conflict-free lane layout: lane l holds elements
-// 128c + 4l .. +3 (c < NC) as two packed bf16 pairs.
-template <int NC>
-struct Row4 {
-    uint2 q[NC];
-    __device__ __forceinline__ void load_smem(const __nv_bfloat16* row, int n, int lane) {
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            const int e = c * 128 + 4 * lane;
-            q[c] = e < n ? *reinterpret_cast<const uint2*>(row + e) : make_uint2(0u, 0u);
-        }
-    }
-    __device__ __forceinline__ void load_global(const __nv_bfloat16* row, int n, int lane, uint64_t pol) {
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-            const int e = c * 128 + 4 * lane;
-            if (e < n)
-                asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
-                             : "=r"(q[c].x), "=r"(q[c].y)
-                             : "l"(row + e), "l"(pol));
-            else
-                q[c] = make_uint2(0u, 0u);
-        }
-    }
-};
-
-// fp32 shared-memory vector chunk c of this lane (zero past n)
-__device__ __forceinline__ float4 vec4(const float* x, int c, int n, int lane) {
-    const int e = c * 128 + 4 * lane;
-    return e < n ? *reinterpret_cast<const float4*>(x + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-__device__ __forceinline__ void fma4(uint2 w, float4 x, float& a0, float& a1) {
-    float w0, w1, w2, w3;
-    bf16x2_to_f32(w.x, w0, w1);
-    bf16x2_to_f32(w.y, w2, w3);
-    a0 = fmaf(w0, x.x, a0);
-    a1 = fmaf(w1, x.y, a1);
-    a0 = fmaf(w2, x.z, a0);
-    a1 = fmaf(w3, x.w, a1);
-}
-
-// Two warp sums at once (their shuffles interleaved).
-__device__ __forceinline__ void warp_sum2(float& a, float& b) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-    }
-}
-
 template <int NC>
 __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     extern __shared__ __align__(128) uint8_t sm[];
