@@ -80,6 +80,7 @@ WORKLOADS = {
     # holds about 2 GB of device memory
     "qwen3_8b_v80k_b1_k0": Workload("qwen3_8b_v80k_b1_k0", QWEN3_8B_V80K, 1, 0, (1,)),
     "qwen3_8b_v80k_b1_k2048": Workload("qwen3_8b_v80k_b1_k2048", QWEN3_8B_V80K, 1, 2048, (1,)),
+    "qwen3_8b_v80k_b64_k0": Workload("qwen3_8b_v80k_b64_k0", QWEN3_8B_V80K, 64, 0, _seeds(64, 1)),
 }
 
 WEIGHT_NAMES = ("lm_head", "emb", "w_ih", "w_hh", "fc1", "fc2", "b")
