@@ -158,12 +158,14 @@ DOMINO_API int domino_rollout_debug_run(domino_ctx* ctx, const void* hidden, con
 
 /* Driver of the 14 dependent steps.  The persistent drivers are one
  * cooperative launch (one CTA per SM).  The tagged-exchange one covers bf16,
- * B <= 4 (B = 1 for the full vocabulary), G, F <= 1024 and V < 2^18: its CTAs
- * pass activations, hidden-side products and per-CTA bests through words
- * that carry the step they belong to, instead of meeting at grid barriers.
+ * B <= 8 (B = 1 for the full vocabulary), G, F <= 1024 and V < 2^18: its CTAs
+ * pass activations, GRU state units and per-CTA bests through words that
+ * carry the step they belong to, instead of meeting at grid barriers.
  * DOMINO_DRIVER_PERSISTENT takes it where it applies and the grid-barrier
  * kernel elsewhere; DOMINO_DRIVER_PERSISTENT_GRID always the latter.  A
- * persistent driver that does not cover the run gives UNSUPPORTED. */
+ * persistent driver that does not cover the run gives UNSUPPORTED.  AUTO
+ * takes a persistent driver for one request and the tagged-exchange one for
+ * pools of up to four requests; other batches run one launch per phase. */
 #define DOMINO_DRIVER_AUTO            0  /* pick per (B, K)                              */
 #define DOMINO_DRIVER_KERNELS         1  /* one launch per phase, stream-ordered         */
 #define DOMINO_DRIVER_PERSISTENT      2  /* one cooperative launch (see above)           */

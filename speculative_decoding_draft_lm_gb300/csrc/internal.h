@@ -114,7 +114,7 @@ bool persist_supported(const domino_ctx* c, const RunArgs& r);
 cudaError_t launch_persist(domino_ctx* c, RunArgs& r);
 
 // persistent driver with tagged data exchanges for small batches (persist_ll.cu)
-constexpr int kLLMaxBatch = 4;        // requests it covers
+constexpr int kLLMaxBatch = 8;        // requests it covers
 constexpr int kClaimCounters = 16;    // sync words 16..31: per-step shared-chunk counters (cleared per run)
 constexpr int kRunEpochWord = 64;     // sync word 64: run counter (bumped per run, never cleared)
 bool persist_ll_supported(const domino_ctx* c, const RunArgs& r);

@@ -1,4 +1,4 @@
-// Persistent driver for small batches (B <= 4, bf16) whose CTAs exchange
+// Persistent driver for small batches (B <= 8, bf16) whose CTAs exchange
 // data through step-tagged words instead of meeting at grid barriers.
 //
 // Per corrected step k (page "Add correctness-first Domino support to DFlash
@@ -26,13 +26,17 @@
 // waits for (e.g. one without projector rows) may still be reading step k's
 // words when a faster CTA publishes step k+1, but no CTA can publish step
 // k+2 before every CTA has published something that follows its reading of
-// step k, so a buffer is never overwritten while it is read.
+// step k, so a buffer is never overwritten while it is read.  A reader
+// loads several words at once and reads the ones without the tag again
+// together, so a late word costs one more L2 round trip, not one per word.
 //
 // Dot products use a lane layout without shared-memory bank conflicts: lane
 // l holds elements 128c + 4l .. 128c + 4l + 3 of a row or vector.  A warp
-// keeps up to two weight rows in registers and streams the state through
-// 16-byte shared loads.  The fc1 rows of a CTA, and for pools its W_hh rows
-// and pool rows, stay in shared memory for the whole launch.  Over the full
+// keeps up to two weight rows in registers, streams every request's state
+// through 16-byte shared loads, and reduces all its (row, request) dots in
+// one transposed butterfly.  The fc1 rows of a CTA, and for pools its W_hh
+// rows and pool rows (as many as fit), stay in shared memory for the whole
+// launch.  Over the full
 // vocabulary a producer warp streams fc2 with bulk copies into a ring
 // (walking the slice in alternating directions so a step starts on the rows
 // the last one read); the last seventh of every slice is shared: producers
@@ -42,6 +46,8 @@
 // Every wait (exchange word, ring slot) is bounded; on a timeout the kernel
 // raises the device error word, and all consumer warps leave together (the
 // decision is taken with a barrier that ORs their flags).
+#include <type_traits>
+
 #include "internal.h"
 #include "persist_util.cuh"
 
@@ -125,41 +131,8 @@ __device__ __forceinline__ bool has_tag(unsigned long long w, unsigned tag, int 
     return mode == 0 ? (unsigned)(w >> 32) == tag : (unsigned)(w & kBestTagMask) == tag;
 }
 
-// Spin until the word at p carries `tag`; bounded.  Returns the last word
-// read: without the tag on a timeout (which also raises the CTA's abort flag
-// and the device error word) or when another thread of the CTA gave up.
-// Out of line: the common case (the word has arrived) never calls it.
-__device__ __noinline__ unsigned long long poll_slow(const unsigned long long* p, unsigned tag, int mode,
-                                                     volatile int* abort_flag, int* err) {
-    const unsigned long long t0 = tc::globaltimer();
-    unsigned long long v;
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i) {
-            __nanosleep(64);  // every spinning thread of every CTA polls L2: keep its request rate down
-            v = ld_relaxed_u64(p);
-            if (has_tag(v, tag, mode)) return v;
-        }
-        if (*abort_flag) return v;
-        if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(err, kErrTimeout);
-            return v;
-        }
-    }
-}
-
-// The word at p with `tag`, given a first read v; sets `failed` if it never came.
-__device__ __forceinline__ unsigned long long poll_word(const unsigned long long* p, unsigned long long v,
-                                                        unsigned tag, int mode, volatile int* abort_flag, int* err,
-                                                        bool& failed) {
-    if (has_tag(v, tag, mode)) return v;
-    v = poll_slow(p, tag, mode, abort_flag, err);
-    if (!has_tag(v, tag, mode)) failed = true;
-    return v;
-}
-
-template <int NC>
+// NC: 128-element chunks of a row per lane; MB: requests a lane tracks bests for
+template <int NC, int MB>
 __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     extern __shared__ __align__(128) uint8_t sm[];
     const int B = p.B, V = p.V, G = p.G, F = p.F;
@@ -356,9 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     };
 
     // ---- projector items of this CTA: its fc1 rows (item < fn, k > 0) and
-    // its units' W_hh rows (item >= fn, when gh is set).  A warp takes two
-    // items at a time with their rows in registers and streams each
-    // request's state from shared memory once for both.
+    // its units' W_hh rows (item >= fn, when gh is set).  A warp takes one
+    // item, or two consecutive items, with the rows in registers, forms the
+    // lane-partial dots with every request's state (streamed from shared
+    // memory once per chunk for both rows), reduces all of them in one
+    // transposed butterfly, and finishes them on as many lanes at once.
+    // With the W_hh rows resident, the fc1 rows (whose activations the other
+    // CTAs wait for) get a pass of their own, one per warp, before the W_hh
+    // pairs; otherwise one pass of pairs covers all items (the W_hh rows read
+    // from L2 are then requested as early as possible).
     auto project = [&](int k, bool gh, bool pub_a, unsigned tag_a, unsigned long long* xa_k) {
         const int nf = k > 0 ? fn : 0;
         const int n_items = nf + (gh ? 3 * jn : 0);
@@ -382,34 +361,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 sgh[(b * 3 + gate) * p.jpc + jj] = v;
             }
         };
-        // fc1 items first (the activations are on the critical path), then
-        // the W_hh items; a warp pairs items of the same kind
-        auto run = [&](int lo, int hi) {
-            for (int it0 = lo + warp; it0 < hi; it0 += 2 * kConsumerWarps) {
-                const int it1 = it0 + kConsumerWarps;
-                const bool two = it1 < hi;
-                Row4<NC> r0, r1;
-                load(it0, r0);
-                if (two) load(it1, r1);
-                for (int b = 0; b < B; ++b) {
-                    float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+        // items [lo, hi), one (TWO = false) or two per warp
+        auto pass = [&](auto two_c, int lo, int hi) {
+            constexpr bool TWO = decltype(two_c)::value;
+            constexpr int NR = TWO ? 2 : 1;
+            constexpr int NV = NR * MB;  // v[r * MB + b]: row r of the warp's items, request b
+            for (int it0 = lo + NR * warp; it0 < hi; it0 += NR * kConsumerWarps) {
+                const bool two = TWO && it0 + 1 < hi;
+                Row4<NC> r[NR];
+                load(it0, r[0]);
+                if (TWO) {
+                    if (two) load(it0 + 1, r[NR - 1]);
+                    else r[NR - 1].zero();
+                }
+                float v[NV];
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        const float4 x = vec4(sh + b * G, c, G, lane);
-                        fma4(r0.q[c], x, a0, a1);
-                        if (two) fma4(r1.q[c], x, c0, c1);
+                for (int i = 0; i < NV; ++i) v[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    float w[NR][4];
+#pragma unroll
+                    for (int rr = 0; rr < NR; ++rr) {
+                        bf16x2_to_f32(r[rr].q[c].x, w[rr][0], w[rr][1]);
+                        bf16x2_to_f32(r[rr].q[c].y, w[rr][2], w[rr][3]);
                     }
-                    float d0 = a0 + a1, d1 = c0 + c1;
-                    warp_sum2(d0, d1);
-                    if (lane == 0) {
-                        finish(it0, b, d0);
-                        if (two) finish(it1, b, d1);
+#pragma unroll
+                    for (int b = 0; b < MB; ++b) {
+                        if (b < B) {
+                            const float4 x = vec4(sh + b * G, c, G, lane);
+#pragma unroll
+                            for (int rr = 0; rr < NR; ++rr)
+                                v[rr * MB + b] = fmaf(w[rr][0], x.x,
+                                                      fmaf(w[rr][1], x.y,
+                                                           fmaf(w[rr][2], x.z, fmaf(w[rr][3], x.w, v[rr * MB + b]))));
+                        }
                     }
+                }
+                const float t = warp_sum_tr<NV>(v, lane);
+                if (tr_reporter<NV>(lane)) {
+                    const int idx = tr_index<NV>(lane), rr = idx / MB, b = idx % MB;
+                    if (b < B && (rr == 0 || two)) finish(it0 + rr, b, t);
                 }
             }
         };
-        run(0, nf);
-        run(nf, n_items);
+        if (p.wh_res) {
+            pass(std::false_type{}, 0, nf);
+            pass(std::true_type{}, nf, n_items);
+        } else {
+            pass(std::true_type{}, 0, n_items);
+        }
     };
 
     // ---- update u of this CTA's units: h[j] = GRU(token-table row, kept
@@ -428,24 +428,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             if (p.dbg_h) p.dbg_h[((size_t)b * kProposals + u) * G + j] = h;
         }
     };
-    // ---- the whole state after update u, from every CTA's published units
-    auto read_state = [&](unsigned tag, const unsigned long long* xh_u) {
-        constexpr int kNT = kConsumerWarps * 32;
-        for (int base = 0; base < B * G; base += 4 * kNT) {
-            unsigned long long w[4];
+    // ---- `count` tagged words, word i at addr(i): four loads per thread
+    // in flight (eight for more than four requests); the words that do not carry the tag yet are read again
+    // together (one L2 round trip per retry round for all of them), with a
+    // short back-off between rounds; bounded.  consume(i, word) for each.
+    auto gather = [&](int count, auto addr, unsigned tag, int mode, auto consume) {
+        constexpr int kNT = kConsumerWarps * 32, kDepth = MB > 4 ? 8 : 4;
+        for (int base = 0; base < count; base += kDepth * kNT) {
+            unsigned long long w[kDepth];
+            unsigned miss = 0u;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < kDepth; ++e) {
                 const int i = base + e * kNT + tid;
-                w[e] = i < B * G ? ld_relaxed_u64(xh_u + i) : 0ull;
+                w[e] = 0ull;
+                if (i < count) {
+                    w[e] = ld_relaxed_u64(addr(i));
+                    miss |= 1u << e;
+                }
+            }
+            unsigned long long t0 = 0ull;
+            for (unsigned round = 0;; ++round) {
+#pragma unroll
+                for (int e = 0; e < kDepth; ++e)
+                    if (((miss >> e) & 1u) && has_tag(w[e], tag, mode)) miss &= ~(1u << e);
+                if (!miss) break;
+                if ((round & 15u) == 15u) {  // the abort flag and the clock, every 16 rounds
+                    if (*abort_flag) {
+                        failed = true;
+                        break;
+                    }
+                    const unsigned long long now = tc::globaltimer();
+                    if (t0 == 0ull) {
+                        t0 = now;
+                    } else if (now - t0 > tc::kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, kErrTimeout);
+                        failed = true;
+                        break;
+                    }
+                }
+                __nanosleep(32);  // every waiting thread of every CTA polls L2: keep its request rate down
+#pragma unroll
+                for (int e = 0; e < kDepth; ++e)
+                    if ((miss >> e) & 1u) w[e] = ld_relaxed_u64(addr(base + e * kNT + tid));
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < kDepth; ++e) {
                 const int i = base + e * kNT + tid;
-                if (i < B * G)
-                    sh[i] = __uint_as_float((unsigned)poll_word(xh_u + i, w[e], tag, 0, abort_flag, p.err, failed));
+                if (i < count && !((miss >> e) & 1u)) consume(i, w[e]);
             }
         }
     };
+    // n tagged fp32 payloads into dst
+    auto read_tagged = [&](const unsigned long long* src, float* dst, int n, unsigned tag) {
+        gather(
+            n, [&](int i) { return src + i; }, tag, 0,
+            [&](int i, unsigned long long w) { dst[i] = __uint_as_float((unsigned)w); });
+    };
+    // ---- the whole state after update u, from every CTA's published units
+    auto read_state = [&](unsigned tag, const unsigned long long* xh_u) { read_tagged(xh_u, sh, B * G, tag); };
 
     // ---- seed update 0 (h_{-1} = 0): the verified token only, independent
     // of the previous kernel; every CTA computes the whole state
@@ -607,31 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         project(k, k < p.n_corr, publish_ok(), tag_k, xa_of(k));
         stamp();  // 3 + 4(k-1): projector published
         // ---- C_k: all activations, then this CTA's slice
-        {
-            constexpr int kNT = kConsumerWarps * 32;
-            const unsigned long long* xa = xa_of(k);
-            for (int base = 0; base < B * F; base += 4 * kNT) {
-                unsigned long long w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = base + e * kNT + tid;
-                    w[e] = i < B * F ? ld_relaxed_u64(xa + i) : 0ull;
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = base + e * kNT + tid;
-                    if (i < B * F)
-                        sa[i] = __uint_as_float((unsigned)poll_word(xa + i, w[e], tag_k, 0, abort_flag, p.err, failed));
-                }
-            }
-        }
+        read_tagged(xa_of(k), sa, B * F, tag_k);
         cp_async_wait_all();
         if (cons_sync_or(failed)) return;
         areg_b = -1;
         stamp();  // 4 + 4(k-1): activations in
-        unsigned long long m[kLLMaxBatch];  // this lane's best per request of the rows it finishes
+        unsigned long long m[MB];  // this lane's best per request of the rows it finishes
 #pragma unroll
-        for (int b = 0; b < kLLMaxBatch; ++b) m[b] = 0ull;
+        for (int b = 0; b < MB; ++b) m[b] = 0ull;
         // one loop for both layouts (a single copy of the slot code): resident
         // pool rows, chunk c in slot c; or ring slots, slot q for warp q % n_cons
         {
@@ -686,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                     const float cv = own ? tot + sbias[r] + sL[r] : tot + tail;
                     const unsigned long long key = best_key(cv, v);
 #pragma unroll
-                    for (int bb = 0; bb < kLLMaxBatch; ++bb)
+                    for (int bb = 0; bb < MB; ++bb)
                         if (bb == b) m[bb] = max(m[bb], key);
                     if (p.dbg_scores) {
                         if (full_vocab) p.dbg_scores[(size_t)(k - 1) * V + v] = cv;
@@ -695,7 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 }
             }
         }
-        for (int b = 0; b < B; ++b) {
+#pragma unroll
+        for (int b = 0; b < MB; ++b) {
+            if (b >= B) break;
             const unsigned long long w = warp_max_u64(m[b]);
             if (lane == 0 && w) atomicMax(&sbest_c[b], w);
         }
@@ -713,12 +739,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         // ---- X_k: every CTA's best of step k gives p_{k+1} for every request
         {
             const unsigned kk = (unsigned)k;
-            for (int i = tid; i < grid * B; i += kConsumerWarps * 32) {
-                const int c = i / B, b = i % B;
-                const unsigned long long* x = xbest_of(k) + (size_t)c * kLLMaxBatch + b;
-                const unsigned long long w = poll_word(x, ld_relaxed_u64(x), kk, 1, abort_flag, p.err, failed);
-                if (w > kBestTagMask) atomicMax(&sbest_x[b], w & ~(unsigned long long)kBestTagMask);
-            }
+            const unsigned long long* xb = xbest_of(k);
+            gather(
+                grid * B, [&](int i) { return xb + (size_t)(i / B) * kLLMaxBatch + i % B; }, kk, 1,
+                [&](int i, unsigned long long w) {
+                    if (w > kBestTagMask) atomicMax(&sbest_x[i % B], w & ~(unsigned long long)kBestTagMask);
+                });
             cons_sync();
             if (tid < B) {
                 const unsigned long long w = sbest_x[tid];
@@ -848,10 +874,14 @@ cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r) {
     c->drop_barrier = 0;
 
     const int mx = g.G > g.F ? g.G : g.F;
-    void (*kern)(LLParams) = mx <= 128   ? k_rollout_ll<1>
-                             : mx <= 256 ? k_rollout_ll<2>
-                             : mx <= 512 ? k_rollout_ll<4>
-                                         : k_rollout_ll<8>;
+    // rows of up to 256, 512 or 1024 elements; one, up to four or up to eight requests
+    auto pick = [&](auto mb) -> void (*)(LLParams) {
+        constexpr int MB = decltype(mb)::value;
+        return mx <= 256 ? k_rollout_ll<2, MB> : mx <= 512 ? k_rollout_ll<4, MB> : k_rollout_ll<8, MB>;
+    };
+    void (*kern)(LLParams) = r.B == 1   ? pick(std::integral_constant<int, 1>{})
+                             : r.B <= 4 ? pick(std::integral_constant<int, 4>{})
+                                        : pick(std::integral_constant<int, kLLMaxBatch>{});
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

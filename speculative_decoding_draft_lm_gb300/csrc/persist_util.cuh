@@ -162,6 +162,10 @@ struct Row4 {
             q[c] = e < n ? *reinterpret_cast<const uint2*>(row + e) : make_uint2(0u, 0u);
         }
     }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) q[c] = make_uint2(0u, 0u);
+    }
     __device__ __forceinline__ void load_global(const __nv_bfloat16* row, int n, int lane, uint64_t pol) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
@@ -198,6 +202,43 @@ __device__ __forceinline__ void warp_sum2(float& a, float& b) {
         a += __shfl_xor_sync(0xffffffffu, a, o);
         b += __shfl_xor_sync(0xffffffffu, b, o);
     }
+}
+
+// Sum each of N per-lane values (N a power of two, N <= 32) over the warp
+// with a transposed butterfly: N - 1 + (5 - log2 N) shuffles instead of
+// 5 N.  At each halving step a lane keeps the half of its values selected
+// by one bit of its lane id and sends the other half to its partner.  Lane l
+// ends with the total of value tr_index<N>(l), which lanes that differ only
+// in the bits below the selecting ones hold as well.
+template <int N>
+__device__ __forceinline__ float warp_sum_tr(float (&v)[N], int lane) {
+#pragma unroll
+    for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float send = up ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 / N; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+template <int N>
+__device__ __forceinline__ int tr_index(int lane) {
+    int idx = 0;
+#pragma unroll
+    for (int n = N, o = 16; n > 1; n >>= 1, o >>= 1)
+        if (lane & o) idx += n / 2;
+    return idx;
+}
+// The lanes that report the values of warp_sum_tr<N>: one per value.
+template <int N>
+__device__ __forceinline__ bool tr_reporter(int lane) {
+    return (lane & (32 / N - 1)) == 0;
 }
 
 }  // namespace persist

@@ -19,7 +19,7 @@ def _scales(sh):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("B,K", [(1, 0), (1, 100), (3, 100), (5, 7)])
+@pytest.mark.parametrize("B,K", [(1, 0), (1, 100), (3, 100), (5, 7), (8, 100)])
 def test_persistent_matches_kernels_and_oracle(dtype, B, K):
     from speculative_decoding_draft_lm_gb300 import rollout as R
     sh = inputs.small_shape(dtype=dtype)
