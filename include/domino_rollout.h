@@ -165,7 +165,7 @@ DOMINO_API int domino_rollout_debug_run(domino_ctx* ctx, const void* hidden, con
  * kernel elsewhere; DOMINO_DRIVER_PERSISTENT_GRID always the latter.  A
  * persistent driver that does not cover the run gives UNSUPPORTED.  AUTO
  * takes a persistent driver for one request and the tagged-exchange one for
- * pools of up to four requests; other batches run one launch per phase. */
+ * the pools it covers; other batches run one launch per phase. */
 #define DOMINO_DRIVER_AUTO            0  /* pick per (B, K)                              */
 #define DOMINO_DRIVER_KERNELS         1  /* one launch per phase, stream-ordered         */
 #define DOMINO_DRIVER_PERSISTENT      2  /* one cooperative launch (see above)           */

@@ -94,10 +94,10 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     } else if (c->driver == DOMINO_DRIVER_PERSISTENT_GRID) {
         persist_kind = persist_supported(c, r) ? 1 : -1;
     } else if (c->driver == DOMINO_DRIVER_AUTO) {
-        // one request: a persistent driver; pools of up to four requests: the
+        // one request: a persistent driver; pools of up to eight requests: the
         // tagged-exchange driver; other batches: the batched kernels
         if (r.B == 1) persist_kind = persist_ll_supported(c, r) ? 2 : persist_supported(c, r) ? 1 : 0;
-        else if (r.K > 0 && r.B <= 4 && persist_ll_supported(c, r)) persist_kind = 2;
+        else if (r.K > 0 && persist_ll_supported(c, r)) persist_kind = 2;
     }
     if (persist_kind < 0) return DOMINO_ERR_UNSUPPORTED;
     const bool use_persist = persist_kind > 0;

@@ -62,6 +62,7 @@ constexpr int kMaxSlots = 64;
 constexpr int kShareDiv = 7;       // a seventh of each full-vocabulary slice is shared
 constexpr int kProducerLanes = 4;  // lanes of the producer warp that issue copies
 constexpr int kMaxSeg = 2048;
+constexpr int kPad = 8;            // elements after each resident row and each state row (bank spread)
 constexpr unsigned kBestTagMask = 0x3FFFu;  // low 14 bits of a best word: the step
 constexpr int kBestIdShift = 14;            // next 18 bits: ~id
 
@@ -89,21 +90,25 @@ struct LLParams {
 };
 
 struct LLLayout {
-    int ring, bars, srow, swhh, sfc1, sh, sa, sL, sbias, spid, ss, sgh, sred, stok, misc, total;
+    int ring, bars, srow, swhh, sfc1, sh, spart, sa, sL, sbias, spid, sqid, ss, sgh, sred, stok, misc, total;
     __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B,
                                  bool wh_res) {
         auto up = [](int x) { return (x + 127) & ~127; };
+        const int rs = G + kPad;                       // row stride of the resident rows and of the state
+        const int mt = (fpc + 3 * jpc + 15) / 16;      // 16-row tiles of the tensor-core projector
         int o = 0;
         ring = o;  o = up(o + n_slots * slot_bytes);
         bars = o;  o = up(o + 16 * n_slots);
         srow = o;  o = up(o + 4 * n_slots);
-        swhh = o;  o = up(o + (wh_res ? 3 * jpc * G * 2 : 0));
-        sfc1 = o;  o = up(o + fpc * G * 2);
-        sh = o;    o = up(o + 4 * B * G);
+        swhh = o;  o = up(o + (wh_res ? 3 * jpc * rs * 2 : 0));
+        sfc1 = o;  o = up(o + fpc * rs * 2);
+        sh = o;    o = up(o + 4 * B * rs);
+        spart = o; o = up(o + (wh_res ? 4 * 128 * (mt > kConsumerWarps ? mt : kConsumerWarps) : 0));
         sa = o;    o = up(o + 4 * B * F);
         sL = o;    o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
         spid = o;  o = up(o + 4 * seg);                   // pool ids of the slice
+        sqid = o;  o = up(o + 4 * seg);                   // the same, for the producer warp
         ss = o;    o = up(o + 4 * B * kProposals * fpc);  // s entries of the CTA's projector outputs
         sgh = o;   o = up(o + 4 * B * 3 * jpc);           // hidden-side products of the CTA's units
         sred = o;  o = up(o + 8 * 2 * kLLMaxBatch);
@@ -144,7 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     volatile int* srow = reinterpret_cast<volatile int*>(sm + lay.srow);
     const __nv_bfloat16* swhh = reinterpret_cast<const __nv_bfloat16*>(sm + lay.swhh);
     const __nv_bfloat16* sfc1 = reinterpret_cast<const __nv_bfloat16*>(sm + lay.sfc1);
-    float* sh = reinterpret_cast<float*>(sm + lay.sh);
+    float* sh = reinterpret_cast<float*>(sm + lay.sh);  // [B][SS] the state (fp32)
+    float* spart = reinterpret_cast<float*>(sm + lay.spart);
+    const int RS = G + kPad, SS = G + kPad;
     float* sa = reinterpret_cast<float*>(sm + lay.sa);
     float* sL = reinterpret_cast<float*>(sm + lay.sL);
     float* sbias = reinterpret_cast<float*>(sm + lay.sbias);
@@ -189,9 +196,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     // lane keeps the same count of slots issued while the copies (and the
     // waits for free slots) of a round proceed in parallel.
     if (warp == kConsumerWarps) {
+        int* sqid = reinterpret_cast<int*>(sm + lay.sqid);
+        if (!full_vocab) {
+            pdl_wait();  // the pool ids come from the previous kernel
+            // the slice's pool ids, read from global memory once (not before every copy)
+            for (int i = lane; i < nw; i += 32) sqid[i] = p.pool[w0 + i];
+            __syncwarp();
+        }
         if (lane >= kProducerLanes) return;
         constexpr unsigned kLanes = (1u << kProducerLanes) - 1u;
-        if (!full_vocab) pdl_wait();  // the pool ids come from the previous kernel
         const uint64_t pol = full_vocab ? tc::policy_evict_normal() : tc::policy_evict_last();
         int q = 0;        // slots issued so far (same in every lane)
         bool ok = true;   // same in every lane
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                     tc::bulk_load(dst, p.fc2 + (size_t)item0 * F, (uint32_t)(nr * row_bytes), full0 + 8 * slot, pol);
                 } else {
                     for (int r = 0; r < nr; ++r)
-                        tc::bulk_load(dst + (uint32_t)(r * row_bytes), p.fc2 + (size_t)p.pool[item0 + r] * F,
+                        tc::bulk_load(dst + (uint32_t)(r * row_bytes), p.fc2 + (size_t)sqid[item0 - w0 + r] * F,
                                       (uint32_t)row_bytes, full0 + 8 * slot, pol);
                 }
             }
@@ -294,14 +307,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         for (int i = tid; i < (p.wh_res ? 3 * jn * per_row : 0); i += kConsumerWarps * 32) {
             const int rr = i / per_row, e = (i % per_row) * 8;
             const int gate = rr / jn, jj = rr % jn;
-            cp_async16((void*)(swhh + ((size_t)gate * p.jpc + jj) * G + e),
+            cp_async16((void*)(swhh + ((size_t)gate * p.jpc + jj) * RS + e),
                        p.w_hh + ((size_t)gate * G + j0 + jj) * G + e);
         }
         for (int i = tid; i < fn * per_row; i += kConsumerWarps * 32) {
             const int rr = i / per_row, e = (i % per_row) * 8;
-            cp_async16((void*)(sfc1 + (size_t)rr * G + e), p.fc1 + (size_t)(f0 + rr) * G + e);
+            cp_async16((void*)(sfc1 + (size_t)rr * RS + e), p.fc1 + (size_t)(f0 + rr) * G + e);
         }
         cp_async_commit();
+        // zero padding after every resident row and state row (a tensor-core
+        // k-step may run past G when G is not a multiple of 16)
+        __nv_bfloat16* zw = reinterpret_cast<__nv_bfloat16*>(sm + lay.swhh);
+        __nv_bfloat16* zf = reinterpret_cast<__nv_bfloat16*>(sm + lay.sfc1);
+        for (int i = tid; i < (p.wh_res ? 3 * p.jpc : 0) + p.fpc + B; i += kConsumerWarps * 32) {
+            const int n1 = p.wh_res ? 3 * p.jpc : 0;
+            if (i < n1) *reinterpret_cast<uint4*>(zw + (size_t)i * RS + G) = make_uint4(0u, 0u, 0u, 0u);
+            else if (i < n1 + p.fpc) *reinterpret_cast<uint4*>(zf + (size_t)(i - n1) * RS + G) = make_uint4(0u, 0u, 0u, 0u);
+            else {
+                float4* z = reinterpret_cast<float4*>(sh + (size_t)(i - n1 - p.fpc) * SS + G);
+                z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
     }
     if (full_vocab)
         for (int i = tid; i < nw; i += kConsumerWarps * 32) sbias[i] = __bfloat162float(p.bias[w0 + i]);
@@ -334,19 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     // lane-partial dots with every request's state (streamed from shared
     // memory once per chunk for both rows), reduces all of them in one
     // transposed butterfly, and finishes them on as many lanes at once.
-    // With the W_hh rows resident, the fc1 rows (whose activations the other
-    // CTAs wait for) get a pass of their own, one per warp, before the W_hh
-    // pairs; otherwise one pass of pairs covers all items (the W_hh rows read
-    // from L2 are then requested as early as possible).
+    // This path serves the rows read from L2 (the W_hh rows over the full
+    // vocabulary): one pass of pairs requests them as early as possible.
     auto project = [&](int k, bool gh, bool pub_a, unsigned tag_a, unsigned long long* xa_k) {
         const int nf = k > 0 ? fn : 0;
         const int n_items = nf + (gh ? 3 * jn : 0);
         auto load = [&](int it, Row4<NC>& r) {
             if (it < nf) {
-                r.load_smem(sfc1 + (size_t)it * G, G, lane);
+                r.load_smem(sfc1 + (size_t)it * RS, G, lane);
             } else {
                 const int g = it - nf, gate = g / jn, jj = g % jn;
-                if (p.wh_res) r.load_smem(swhh + ((size_t)gate * p.jpc + jj) * G, G, lane);
+                if (p.wh_res) r.load_smem(swhh + ((size_t)gate * p.jpc + jj) * RS, G, lane);
                 else r.load_global(p.w_hh + ((size_t)gate * G + j0 + jj) * G, G, lane, pol_keep);
             }
         };
@@ -388,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
 #pragma unroll
                     for (int b = 0; b < MB; ++b) {
                         if (b < B) {
-                            const float4 x = vec4(sh + b * G, c, G, lane);
+                            const float4 x = vec4(sh + b * SS, c, G, lane);
 #pragma unroll
                             for (int rr = 0; rr < NR; ++rr)
                                 v[rr * MB + b] = fmaf(w[rr][0], x.x,
@@ -404,11 +429,64 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 }
             }
         };
-        if (p.wh_res) {
-            pass(std::false_type{}, 0, nf);
-            pass(std::true_type{}, nf, n_items);
+        // All rows resident: the items as 16-row tiles on the tensor cores
+        // (mma m16n8k16, one column per request).  A warp takes a (tile,
+        // k-range) unit: the rows come from shared memory with ldmatrix, the
+        // state as bf16 leading parts and remainders (two products per
+        // k-step, fp32 accumulation); the units' partial tiles are summed
+        // through shared memory and finished one output per thread.
+        auto tc_pass = [&]() {
+            if (n_items == 0) return;  // the same in every warp of the CTA
+            const int mt = (n_items + 15) / 16;
+            const int nkr = mt >= kConsumerWarps ? 1 : kConsumerWarps / mt;
+            const int ks = (G + 15) / 16;
+            const int mi = lane >> 3, rl = (lane & 7) + (mi & 1) * 8, kofs = (mi >> 1) * 8;
+            const float* xrow = sh + (size_t)min(lane >> 2, B - 1) * SS + (lane & 3) * 2;
+            for (int u = warp; u < mt * nkr; u += kConsumerWarps) {
+                const int m = u / nkr, r = u % nkr;
+                const int it = min(m * 16 + rl, n_items - 1);  // rows past the items repeat the last one
+                const __nv_bfloat16* arow;
+                if (it < nf) {
+                    arow = sfc1 + (size_t)it * RS;
+                } else {
+                    const int g = it - nf, gate = g / jn, jj = g % jn;
+                    arow = swhh + ((size_t)gate * p.jpc + jj) * RS;
+                }
+                const uint32_t abase = tc::smem_u32(arow + kofs);
+                const int kq1 = (r + 1) * ks / nkr;
+                float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int kq = r * ks / nkr; kq < kq1; ++kq) {
+                    uint32_t a[4];
+                    ldmatrix_x4(abase + (uint32_t)kq * 32u, a);
+                    const float2 x01 = *reinterpret_cast<const float2*>(xrow + kq * 16);
+                    const float2 x23 = *reinterpret_cast<const float2*>(xrow + kq * 16 + 8);
+                    uint32_t h0, l0, h1, l1;
+                    split_bf16x2(x01.x, x01.y, h0, l0);
+                    split_bf16x2(x23.x, x23.y, h1, l1);
+                    mma_16816(d0, a, h0, h1);
+                    mma_16816(d1, a, l0, l1);
+                }
+                float* pt = spart + (size_t)u * 128;
+                const int row = lane >> 2, col = (lane & 3) * 2;
+                *reinterpret_cast<float2*>(pt + row * 8 + col) = make_float2(d0[0] + d1[0], d0[1] + d1[1]);
+                *reinterpret_cast<float2*>(pt + (row + 8) * 8 + col) = make_float2(d0[2] + d1[2], d0[3] + d1[3]);
+            }
+            cons_sync();
+            for (int o = tid; o < mt * 128; o += kConsumerWarps * 32) {
+                const int m = o >> 7, row = (o >> 3) & 15, col = o & 7, it = m * 16 + row;
+                if (it < n_items && col < B) {
+                    const float* pt = spart + (size_t)m * nkr * 128 + row * 8 + col;
+                    float v = 0.f;
+                    for (int r = 0; r < nkr; ++r) v += pt[r * 128];
+                    finish(it, col, v);
+                }
+            }
+        };
+        if constexpr (MB > 1) {
+            tc_pass();  // batches run only on pools, whose rows are all resident
         } else {
-            pass(std::true_type{}, 0, n_items);
+            if (p.wh_res) tc_pass();
+            else pass(std::true_type{}, 0, n_items);
         }
     };
 
@@ -423,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             const float r = sigmoidf_(gr + gh[0]);
             const float zg = sigmoidf_(gz + gh[p.jpc]);
             const float n = tanhf(gn + r * gh[2 * p.jpc]);
-            const float h = (1.f - zg) * n + zg * sh[b * G + j];
+            const float h = (1.f - zg) * n + zg * sh[b * SS + j];
             if (pub) st_relaxed_u64(xh_u + (size_t)b * G + j, tagged(h, tag));
             if (p.dbg_h) p.dbg_h[((size_t)b * kProposals + u) * G + j] = h;
         }
@@ -486,7 +564,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             [&](int i, unsigned long long w) { dst[i] = __uint_as_float((unsigned)w); });
     };
     // ---- the whole state after update u, from every CTA's published units
-    auto read_state = [&](unsigned tag, const unsigned long long* xh_u) { read_tagged(xh_u, sh, B * G, tag); };
+    // (word i of the exchange is element i % G of request i / G; the quotient
+    // by a multiply-high with ceil(2^32 / G), exact for i < 2^32 / G)
+    const unsigned g_magic = (unsigned)((0x100000000ull + (unsigned)G - 1u) / (unsigned)G);
+    auto read_state = [&](unsigned tag, const unsigned long long* xh_u) {
+        gather(
+            B * G, [&](int i) { return xh_u + i; }, tag, 0,
+            [&](int i, unsigned long long w) {
+                const int b = (int)__umulhi((unsigned)i, g_magic);
+                sh[b * SS + (i - b * G)] = __uint_as_float((unsigned)w);
+            });
+    };
 
     // ---- seed update 0 (h_{-1} = 0): the verified token only, independent
     // of the previous kernel; every CTA computes the whole state
@@ -509,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         const float zg = sigmoidf_(__ldg(gi + G));
         const float n = tanhf(__ldg(gi + 2 * G));
         const float h = (1.f - zg) * n;
-        sh[b * G + j] = h;
+        sh[b * SS + j] = h;
         if (p.dbg_h && j >= j0 && j < j0 + jn) p.dbg_h[((size_t)b * kProposals + 0) * G + j] = h;
     }
     cp_async_wait_all();

@@ -241,5 +241,34 @@ __device__ __forceinline__ bool tr_reporter(int lane) {
     return (lane & (32 / N - 1)) == 0;
 }
 
+// ---- warp-level bf16 tensor-core products (m16n8k16, fp32 accumulate)
+// Four 8x8 bf16 matrices from shared memory; lane l gives the address of row
+// l % 8 of matrix l / 8 (16-byte aligned) and receives in register i the
+// elements (row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1) of matrix i.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// d += A (16x16, row-major fragments) * B (16x8, column fragments)
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two fp32 values as a pair of bf16 leading parts (hi, round to nearest) and
+// a pair of bf16 remainders (lo = x - hi, rounded; x - hi itself is exact):
+// |x - hi - lo| <= 2^-16 |x|, and the products of a bf16 weight with hi and
+// with lo are exact in fp32, so w*hi + w*lo differs from w*x by at most
+// 2^-16 |w x| before the accumulation's own rounding.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 }  // namespace persist
 }  // namespace domino
