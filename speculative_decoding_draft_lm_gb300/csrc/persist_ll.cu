@@ -85,13 +85,15 @@ struct LLParams {
     int seg;        // rows (K0) or pool entries per CTA, a multiple of kRows
     int jpc, fpc;   // GRU units / fc1 rows per CTA
     int n_slots, n_cons, resident, pin_gi;
+    int ra;         // requests whose activations a CTA keeps (its slice spans at most this many)
     int wh_res;     // W_hh rows of the CTA's units kept in shared memory (else read from L2 each step)
     int drop_at;    // test hook: CTA 0 withholds its publication number drop_at (0 = never)
 };
 
 struct LLLayout {
     int ring, bars, srow, swhh, sfc1, sh, spart, sa, sL, sbias, spid, sqid, ss, sgh, sred, stok, misc, total;
-    __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B,
+    // ra: requests whose activations a CTA keeps (those its correction slice covers)
+    __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B, int ra,
                                  bool wh_res) {
         auto up = [](int x) { return (x + 127) & ~127; };
         const int rs = G + kPad;                       // row stride of the resident rows and of the state
@@ -104,7 +106,7 @@ struct LLLayout {
         sfc1 = o;  o = up(o + fpc * rs * 2);
         sh = o;    o = up(o + 4 * B * rs);
         spart = o; o = up(o + (wh_res ? 4 * 128 * (mt > kConsumerWarps ? mt : kConsumerWarps) : 0));
-        sa = o;    o = up(o + 4 * B * F);
+        sa = o;    o = up(o + 4 * ra * F);
         sL = o;    o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
         spid = o;  o = up(o + 4 * seg);                   // pool ids of the slice
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     const int B = p.B, V = p.V, G = p.G, F = p.F;
     const size_t row_bytes = (size_t)F * sizeof(__nv_bfloat16);
     const int slot_bytes = kRows * F * (int)sizeof(__nv_bfloat16);
-    const LLLayout lay(p.n_slots, slot_bytes, G, F, p.jpc, p.fpc, p.seg, B, p.wh_res != 0);
+    const LLLayout lay(p.n_slots, slot_bytes, G, F, p.jpc, p.fpc, p.seg, B, p.ra, p.wh_res != 0);
     uint8_t* ring = sm + lay.ring;
     const uint32_t full0 = tc::smem_u32(sm + lay.bars), empty0 = full0 + 8 * p.n_slots;
     volatile int* srow = reinterpret_cast<volatile int*>(sm + lay.srow);
@@ -172,6 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     const long long w1 = min(work, w0 + p.seg);
     const int nw = (int)(w1 - w0);
     const int n_chunks = (nw + kRows - 1) / kRows;
+    // the requests of the slice (a pool slice covers consecutive requests)
+    const int rb0 = full_vocab || nw == 0 ? 0 : (int)(w0 / p.K);
+    const int nra = full_vocab ? 1 : nw == 0 ? 0 : (int)((w1 - 1) / p.K) - rb0 + 1;
     const int n_share = full_vocab ? n_chunks / kShareDiv : 0;
     const int n_static = n_chunks - n_share;
     // GRU units and fc1 rows of this CTA
@@ -284,7 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                         base = __shfl_sync(kLanes, next, 0);
                     }
                 }
-                for (int e0 = 0; e0 < p.n_cons && ok; e0 += kProducerLanes) round(e0 + lane < p.n_cons, -1, 0);
+                // full vocabulary: the per-step count of a CTA's chunks varies with
+                // the claims, so an end marker per consumer warp closes the step
+                // (pools: every step has n_chunks, and the consumers count them)
+                if (full_vocab)
+                    for (int e0 = 0; e0 < p.n_cons && ok; e0 += kProducerLanes) round(e0 + lane < p.n_cons, -1, 0);
             }
         }
         if (lane != 0) return;
@@ -648,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
             const int e = (lane + 32 * cc) * 8;
-            if (e < F) lds8(sa + b * F + e, areg[cc]);
+            if (e < F) lds8(sa + (b - rb0) * F + e, areg[cc]);
         }
         areg_b = b;
     };
@@ -659,6 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         const int bl1 = full_vocab ? 0 : (int)((item0 + nr - 1) / p.K);
         if (bl0 == bl1) {
             if (bl0 != areg_b) load_areg(bl0);
+            // all rows of the slot, also those past nr (in the slot's memory;
+            // their totals are not used): the four 16-byte loads of a chunk
+            // are issued together, then their products
             float acc[kRows][2];
 #pragma unroll
             for (int rr = 0; rr < kRows; ++rr) acc[rr][0] = acc[rr][1] = 0.f;
@@ -666,16 +678,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             for (int cc = 0; cc < NCH; ++cc) {
                 const int e = (lane + 32 * cc) * 8;
                 if (e < F) {
+                    uint4 raw[kRows];
+#pragma unroll
+                    for (int rr = 0; rr < kRows; ++rr) raw[rr] = *reinterpret_cast<const uint4*>(srows + (size_t)rr * F + e);
 #pragma unroll
                     for (int rr = 0; rr < kRows; ++rr) {
-                        if (rr < nr) {
-                            float wv[8];
-                            lds8(srows + (size_t)rr * F + e, wv);
+                        float wv[8];
+                        bf16x2_to_f32(raw[rr].x, wv[0], wv[1]);
+                        bf16x2_to_f32(raw[rr].y, wv[2], wv[3]);
+                        bf16x2_to_f32(raw[rr].z, wv[4], wv[5]);
+                        bf16x2_to_f32(raw[rr].w, wv[6], wv[7]);
 #pragma unroll
-                            for (int i = 0; i < 8; i += 2) {
-                                acc[rr][0] = fmaf(wv[i], areg[cc][i], acc[rr][0]);
-                                acc[rr][1] = fmaf(wv[i + 1], areg[cc][i + 1], acc[rr][1]);
-                            }
+                        for (int i = 0; i < 8; i += 2) {
+                            acc[rr][0] = fmaf(wv[i], areg[cc][i], acc[rr][0]);
+                            acc[rr][1] = fmaf(wv[i + 1], areg[cc][i + 1], acc[rr][1]);
                         }
                     }
                 }
@@ -736,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         project(k, k < p.n_corr, publish_ok(), tag_k, xa_of(k));
         stamp();  // 3 + 4(k-1): projector published
         // ---- C_k: all activations, then this CTA's slice
-        read_tagged(xa_of(k), sa, B * F, tag_k);
+        read_tagged(xa_of(k) + (size_t)rb0 * F, sa, nra * F, tag_k);
         cp_async_wait_all();
         if (cons_sync_or(failed)) return;
         areg_b = -1;
@@ -762,6 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                     }
                     item0 = w0 + slot * kRows;
                 } else {
+                    if (!full_vocab && qw >= k * n_chunks) break;  // this warp's chunks of the step are done
                     const int q = qw;
                     qw += p.n_cons;
                     slot = q % p.n_slots;
@@ -855,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
 }
 
 struct LLPlan {
-    int seg, jpc, fpc, n_slots, n_cons, resident, wh_res, smem;
+    int seg, jpc, fpc, n_slots, n_cons, resident, wh_res, ra, smem;
 };
 
 LLPlan make_ll_plan(const domino_ctx* c, int B, int K) {
@@ -873,7 +890,9 @@ LLPlan make_ll_plan(const domino_ctx* c, int B, int K) {
     // over the full vocabulary the correction phase leaves the hidden-side
     // products plenty of time to read W_hh from L2, and the ring gets the room
     pl.wh_res = K > 0;
-    const LLLayout base(0, slot_bytes, g.G, g.F, pl.jpc, pl.fpc, pl.seg, B, pl.wh_res != 0);
+    // a slice of seg consecutive pool entries spans at most (seg - 1) / K + 2 requests
+    pl.ra = K == 0 ? 1 : ((pl.seg - 1) / K + 2 < B ? (pl.seg - 1) / K + 2 : B);
+    const LLLayout base(0, slot_bytes, g.G, g.F, pl.jpc, pl.fpc, pl.seg, B, pl.ra, pl.wh_res != 0);
     const int avail = max_smem - base.total - 1024;
     const int per_slot = slot_bytes + 20;
     const int chunks = pl.seg / kRows;
@@ -896,7 +915,7 @@ LLPlan make_ll_plan(const domino_ctx* c, int B, int K) {
         pl.n_cons = nc;
     }
     if (pl.n_slots < 1) return pl;
-    pl.smem = LLLayout(pl.n_slots, slot_bytes, g.G, g.F, pl.jpc, pl.fpc, pl.seg, B, pl.wh_res != 0).total;
+    pl.smem = LLLayout(pl.n_slots, slot_bytes, g.G, g.F, pl.jpc, pl.fpc, pl.seg, B, pl.ra, pl.wh_res != 0).total;
     return pl;
 }
 
@@ -954,6 +973,7 @@ cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r) {
     p.fpc = pl.fpc;
     p.n_slots = pl.n_slots;
     p.n_cons = pl.n_cons;
+    p.ra = pl.ra;
     p.resident = pl.resident;
     p.wh_res = pl.wh_res;
     // the candidates' token-table rows stay in L2 when they are a modest share of it
