@@ -229,8 +229,10 @@ DOMINO_API int domino_rollout_status(domino_ctx* ctx, void* cuda_stream);
  * (barriers 1 and 2 follow the two seed updates; each corrected step then
  * has two, or three for more than four requests), or in the tagged-exchange
  * driver its n-th publication (1: its GRU units after the seed update; then
- * per step its activations, its best, and, unless the step is the last, its
- * GRU units after the next update).  Nothing replaces it, so the bounded
+ * per step its activations, together with its units' hidden-side products
+ * for one request, its best, and, for more than one request and unless the
+ * step is the last, its GRU units after the next update).  Nothing replaces
+ * it, so the bounded
  * wait of every CTA for it runs out after 200 ms, the kernel returns, the
  * run's tokens are meaningless and
  * domino_rollout_status() reports DOMINO_ERR_TIMEOUT.  Nothing faults or

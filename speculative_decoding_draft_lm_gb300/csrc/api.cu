@@ -237,6 +237,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oXa = take(ll ? (size_t)2 * kLLMaxBatch * g.F * 8 : 0);
     size_t oXg = take(ll ? (size_t)2 * kLLMaxBatch * g.G * 8 : 0);
     size_t oXb = take(ll ? (size_t)2 * c->num_sms * kLLMaxBatch * 8 : 0);
+    size_t oXq = take(ll ? (size_t)2 * 3 * g.G * 8 : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -264,6 +265,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->xa = ll ? (unsigned long long*)(base + oXa) : nullptr;
     c->xh = ll ? (unsigned long long*)(base + oXg) : nullptr;
     c->xbest = ll ? (unsigned long long*)(base + oXb) : nullptr;
+    c->xg = ll ? (unsigned long long*)(base + oXq) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {

@@ -183,6 +183,7 @@ struct domino_ctx {
     unsigned long long* xa;     // [2][kLLMaxBatch,F] tagged activations (tagged-exchange driver)
     unsigned long long* xh;     // [2][kLLMaxBatch,G] tagged GRU state
     unsigned long long* xbest;  // [2][num_sms,kLLMaxBatch] per-CTA best of a step
+    unsigned long long* xg;     // [2][3G] tagged hidden-side products of every unit (one request)
     float* gi_table;          // [V, 3G] input-side GRU pre-activations of every token (built at load)
     float* gh_next;           // [kPersistGruGroup][3G] hidden-side pre-activations of the next GRU update (persistent driver)
     __nv_bfloat16* wp;        // [4*Gp, G] packed hidden-side GRU weights (bf16 batches), or null

@@ -15,6 +15,9 @@
 //        token-table row's three entries and its kept products, and
 //        publishes them;
 //   H_k  reads the whole new state.
+// For one request the hidden-side products of every unit are published
+// with the activations and read while the bests come in; X_k then updates
+// every unit in each CTA, and H_k (one exchange per step) is not needed.
 //
 // Exchange words are 64 bits: a 32-bit payload with a 32-bit tag (run epoch
 // * 16 + step), or for the per-CTA bests the packed key (orderable value, low
@@ -78,6 +81,7 @@ struct LLParams {
     unsigned long long* xa;     // [2][kLLMaxBatch][F]   activations, by step parity
     unsigned long long* xh;     // [2][kLLMaxBatch][G]   GRU state, by update parity
     unsigned long long* xbest;  // [2][grid][kLLMaxBatch] per-CTA bests, by step parity, zeroed per run
+    unsigned long long* xg;     // [2][3G] hidden-side products of every unit (one request), by step parity
     float *dbg_h, *dbg_z, *dbg_scores;
     unsigned long long* trace;
     int B, K, V, G, F;
@@ -91,7 +95,7 @@ struct LLParams {
 };
 
 struct LLLayout {
-    int ring, bars, srow, swhh, sfc1, sh, spart, sa, sL, sbias, spid, sqid, ss, sgh, sred, stok, misc, total;
+    int ring, bars, srow, swhh, sfc1, sh, spart, sa, sL, sbias, spid, sqid, ss, sgh, sgall, sred, stok, misc, total;
     // ra: requests whose activations a CTA keeps (those its correction slice covers)
     __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B, int ra,
                                  bool wh_res) {
@@ -113,6 +117,7 @@ struct LLLayout {
         sqid = o;  o = up(o + 4 * seg);                   // the same, for the producer warp
         ss = o;    o = up(o + 4 * B * kProposals * fpc);  // s entries of the CTA's projector outputs
         sgh = o;   o = up(o + 4 * B * 3 * jpc);           // hidden-side products of the CTA's units
+        sgall = o; o = up(o + (B == 1 ? 4 * 3 * G : 0));  // one request: those of every unit
         sred = o;  o = up(o + 8 * 2 * kLLMaxBatch);
         stok = o;  o = up(o + 4 * kLLMaxBatch);
         misc = o;  o = up(o + 64);
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     int* spid = reinterpret_cast<int*>(sm + lay.spid);
     float* ss = reinterpret_cast<float*>(sm + lay.ss);
     float* sgh = reinterpret_cast<float*>(sm + lay.sgh);
+    float* sgall = reinterpret_cast<float*>(sm + lay.sgall);
     unsigned long long* sred = reinterpret_cast<unsigned long long*>(sm + lay.sred);
     int* stok = reinterpret_cast<int*>(sm + lay.stok);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + lay.misc);
@@ -372,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     // transposed butterfly, and finishes them on as many lanes at once.
     // This path serves the rows read from L2 (the W_hh rows over the full
     // vocabulary): one pass of pairs requests them as early as possible.
-    auto project = [&](int k, bool gh, bool pub_a, unsigned tag_a, unsigned long long* xa_k) {
+    // xg_k: where the hidden-side products are published as well (one request), or null
+    auto project = [&](int k, bool gh, bool pub_a, unsigned tag_a, unsigned long long* xa_k, unsigned long long* xg_k) {
         const int nf = k > 0 ? fn : 0;
         const int n_items = nf + (gh ? 3 * jn : 0);
         auto load = [&](int it, Row4<NC>& r) {
@@ -393,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             } else {
                 const int g = it - nf, gate = g / jn, jj = g % jn;
                 sgh[(b * 3 + gate) * p.jpc + jj] = v;
+                if (xg_k && pub_a) st_relaxed_u64(xg_k + (size_t)gate * G + j0 + jj, tagged(v, tag_a));
             }
         };
         // items [lo, hi), one (TWO = false) or two per warp
@@ -572,6 +580,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             n, [&](int i) { return src + i; }, tag, 0,
             [&](int i, unsigned long long w) { dst[i] = __uint_as_float((unsigned)w); });
     };
+    // ---- one request, update u of every unit from the token-table row and
+    // every unit's hidden-side products (sgall), in place: each element is
+    // read and written by one thread
+    auto update_all = [&](int u) {
+        constexpr int kNT = kConsumerWarps * 32;
+        const float* gi = p.gi_table + (size_t)stok[0] * 3 * G;
+        for (int j0_ = tid; j0_ < G; j0_ += 4 * kNT) {
+            float gr[4], gz[4], gn[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0_ + e * kNT;
+                if (j < G) {
+                    gr[e] = __ldg(gi + j);
+                    gz[e] = __ldg(gi + G + j);
+                    gn[e] = __ldg(gi + 2 * G + j);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = j0_ + e * kNT;
+                if (j < G) {
+                    const float r = sigmoidf_(gr[e] + sgall[j]);
+                    const float zg = sigmoidf_(gz[e] + sgall[G + j]);
+                    const float n = tanhf(gn[e] + r * sgall[2 * G + j]);
+                    const float h = (1.f - zg) * n + zg * sh[j];
+                    sh[j] = h;
+                    if (p.dbg_h && j >= j0 && j < j0 + jn) p.dbg_h[(size_t)u * G + j] = h;
+                }
+            }
+        }
+    };
     // ---- the whole state after update u, from every CTA's published units
     // (word i of the exchange is element i % G of request i / G; the quotient
     // by a multiply-high with ceil(2^32 / G), exact for i < 2^32 / G)
@@ -611,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     }
     cp_async_wait_all();
     cons_sync();
-    project(0, true, false, 0u, nullptr);  // hidden-side products of update 1
+    project(0, true, false, 0u, nullptr, nullptr);  // hidden-side products of update 1
     stamp();  // 1
     pdl_wait();  // base logits, p_1 and the pool are ready; the run counter is bumped
     const unsigned ep16 = *p.epoch * 16u;
@@ -621,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     auto xh_of = [&](int u) { return p.xh + (size_t)(u & 1) * kLLMaxBatch * G; };
     auto xa_of = [&](int k) { return p.xa + (size_t)(k & 1) * kLLMaxBatch * F; };
     auto xbest_of = [&](int k) { return p.xbest + (size_t)(k & 1) * grid * kLLMaxBatch; };
+    auto xg_of = [&](int k) { return p.xg + (size_t)(k & 1) * 3 * G; };
     if (!full_vocab)
         for (int i = tid; i < nw; i += kConsumerWarps * 32) {
             const int v = p.pool[w0 + i];
@@ -749,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
 
         // ---- P_k: the projector slice (published), and the next update's
         // hidden-side products of this CTA's units (kept)
-        project(k, k < p.n_corr, publish_ok(), tag_k, xa_of(k));
+        project(k, k < p.n_corr, publish_ok(), tag_k, xa_of(k), MB == 1 && k < p.n_corr ? xg_of(k) : nullptr);
         stamp();  // 3 + 4(k-1): projector published
         // ---- C_k: all activations, then this CTA's slice
         read_tagged(xa_of(k) + (size_t)rb0 * F, sa, nra * F, tag_k);
@@ -841,6 +881,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         }
         stamp();  // 5 + 4(k-1): best published
         if (k == p.n_corr && cta != 0) return;  // only CTA 0 reports the last step
+        // one request: every unit's hidden-side products (published with the
+        // activations, long since) while the other CTAs finish their bests
+        if (MB == 1 && k < p.n_corr) read_tagged(xg_of(k), sgall, 3 * G, tag_k);
         // ---- X_k: every CTA's best of step k gives p_{k+1} for every request
         {
             const unsigned kk = (unsigned)k;
@@ -861,11 +904,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         }
         if (cons_sync_or(failed)) return;
         if (k < p.n_corr) {
-            // ---- this CTA's units of h_{k+1}, then (H_k) the whole state
-            update_own(k + 1, publish_ok(), ep16 + (unsigned)(k + 1), xh_of(k + 1));
-            cons_sync();  // every read of the old state is done
-            read_state(ep16 + (unsigned)(k + 1), xh_of(k + 1));
-            if (cons_sync_or(failed)) return;
+            if constexpr (MB == 1) {
+                // ---- one request: the whole h_{k+1} here, no exchange
+                update_all(k + 1);
+                cons_sync();
+            } else {
+                // ---- this CTA's units of h_{k+1}, then (H_k) the whole state
+                update_own(k + 1, publish_ok(), ep16 + (unsigned)(k + 1), xh_of(k + 1));
+                cons_sync();  // every read of the old state is done
+                read_state(ep16 + (unsigned)(k + 1), xh_of(k + 1));
+                if (cons_sync_or(failed)) return;
+            }
         }
         stamp();  // 6 + 4(k-1): next state built
     }
@@ -958,6 +1007,7 @@ cudaError_t launch_persist_ll(domino_ctx* c, RunArgs& r) {
     p.xa = c->xa;
     p.xh = c->xh;
     p.xbest = c->xbest;
+    p.xg = c->xg;
     p.dbg_h = r.dbg.h;
     p.dbg_z = r.dbg.z;
     p.dbg_scores = r.dbg.scores;
