@@ -143,8 +143,12 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     }
 #define GRU(u) (gru_tc ? launch_gru_tc(c, r, gm, (u)) : batch ? launch_gru_batch(c, r, (u)) : launch_gru(c, r, (u)))
 #define FC1(k) (gru_tc ? launch_fc1_tc(c, r, gm, (k)) : batch ? launch_fc1_batch(c, r, (k)) : launch_fc1(c, r, (k)))
+    // bf16 batches of up to eight requests: one fused launch per step (the
+    // GRU update and projector layer 1), after the seed update and W_hh h_0.
+    // A block of one proposal has no step, but still the seed's second update.
+    const bool fused = batch && !gru_tc && r.n_prop >= 2 && step_fused_supported(c, r);
     STEP(DOMINO_PHASE_GRU, GRU(0));
-    STEP(DOMINO_PHASE_GRU, GRU(1));
+    STEP(DOMINO_PHASE_GRU, fused ? launch_step_fused(c, r, 0) : GRU(1));
     {
         // tensor cores once the full-vocabulary correction is a real
         // contraction (two or more requests); CUDA cores for B = 1 and pools
@@ -157,14 +161,14 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         }
         const int n_corr = r.n_prop - 1;
         for (int k = 1; k <= n_corr; ++k) {
-            STEP(DOMINO_PHASE_FC1, FC1(k));
+            STEP(DOMINO_PHASE_FC1, fused ? launch_step_fused(c, r, k) : FC1(k));
             if (tc_corr)
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_tc(c, r, tm_a, k));
             else if (r.K > 0 && batch && pool_batch_supported(c))
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_pool_batch(c, r, k));
             else
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
-            if (k < n_corr) STEP(DOMINO_PHASE_GRU, GRU(k + 1));
+            if (k < n_corr && !fused) STEP(DOMINO_PHASE_GRU, GRU(k + 1));
         }
     }
 #undef GRU
@@ -238,6 +242,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oXg = take(ll ? (size_t)2 * kLLMaxBatch * g.G * 8 : 0);
     size_t oXb = take(ll ? (size_t)2 * c->num_sms * kLLMaxBatch * 8 : 0);
     size_t oXq = take(ll ? (size_t)2 * 3 * g.G * 8 : 0);
+    size_t oGb = take(ll ? (size_t)2 * g.max_B * 3 * g.G * sizeof(float) : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -266,6 +271,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->xh = ll ? (unsigned long long*)(base + oXg) : nullptr;
     c->xbest = ll ? (unsigned long long*)(base + oXb) : nullptr;
     c->xg = ll ? (unsigned long long*)(base + oXq) : nullptr;
+    c->ghb = ll ? (float*)(base + oGb) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {

@@ -87,6 +87,11 @@ bool batch_kernels_supported(const domino_ctx* c);
 // h16_out (nullable [B,G]): also store the new state as bf16 (tensor-core operand)
 cudaError_t launch_gru_batch(domino_ctx* c, RunArgs& r, int u, __nv_bfloat16* h16_out = nullptr);
 cudaError_t launch_fc1_batch(domino_ctx* c, RunArgs& r, int k);
+// one fused launch per step for bf16 batches of up to eight requests
+// (step_fused.cu): launch 0 forms W_hh h_0; launch u >= 1 updates to h_u and
+// projects it (step k = u)
+bool step_fused_supported(const domino_ctx* c, const RunArgs& r);
+cudaError_t launch_step_fused(domino_ctx* c, RunArgs& r, int u);
 bool pool_batch_supported(const domino_ctx* c);
 cudaError_t launch_correct_pool_batch(domino_ctx* c, RunArgs& r, int k);
 
