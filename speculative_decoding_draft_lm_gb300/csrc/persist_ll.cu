@@ -253,6 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 const int c = c0 + lane;
                 round(c < n_chunks, w0 + c * kRows, min(kRows, nw - c * kRows));
             }
+        } else if (!full_vocab) {
+            // pools: step k's chunks are sequence numbers (k-1) n_chunks + i,
+            // and lane l issues i = l, l + 4, ... on its own, so a slot that
+            // frees early is refilled without waiting for the other lanes
+            for (int k = 1; k <= p.n_corr && ok && !*abort_flag; ++k) {
+                const bool fwd = (k & 1) != 0;
+                for (int i = lane; i < n_chunks && ok; i += kProducerLanes) {
+                    const int c = fwd ? i : n_chunks - 1 - i;
+                    ok = issue_at((k - 1) * n_chunks + i, w0 + c * kRows, min(kRows, nw - c * kRows));
+                }
+            }
+            q = p.n_corr * n_chunks;
         } else {
             const unsigned total_claims = (unsigned)((p.seg / kRows) / kShareDiv + 1) * (unsigned)grid;
             for (int k = 1; k <= p.n_corr; ++k) {
@@ -531,13 +543,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         constexpr int kNT = kConsumerWarps * 32, kDepth = MB > 4 ? 8 : 4;
         for (int base = 0; base < count; base += kDepth * kNT) {
             unsigned long long w[kDepth];
+            const unsigned long long* pw[kDepth];  // addresses, formed once
             unsigned miss = 0u;
 #pragma unroll
             for (int e = 0; e < kDepth; ++e) {
                 const int i = base + e * kNT + tid;
                 w[e] = 0ull;
+                pw[e] = nullptr;
                 if (i < count) {
-                    w[e] = ld_relaxed_u64(addr(i));
+                    pw[e] = addr(i);
+                    w[e] = ld_relaxed_u64(pw[e]);
                     miss |= 1u << e;
                 }
             }
@@ -565,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 __nanosleep(32);  // every waiting thread of every CTA polls L2: keep its request rate down
 #pragma unroll
                 for (int e = 0; e < kDepth; ++e)
-                    if ((miss >> e) & 1u) w[e] = ld_relaxed_u64(addr(base + e * kNT + tid));
+                    if ((miss >> e) & 1u) w[e] = ld_relaxed_u64(pw[e]);
             }
 #pragma unroll
             for (int e = 0; e < kDepth; ++e) {
@@ -888,11 +903,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         {
             const unsigned kk = (unsigned)k;
             const unsigned long long* xb = xbest_of(k);
-            gather(
-                grid * B, [&](int i) { return xb + (size_t)(i / B) * kLLMaxBatch + i % B; }, kk, 1,
-                [&](int i, unsigned long long w) {
-                    if (w > kBestTagMask) atomicMax(&sbest_x[i % B], w & ~(unsigned long long)kBestTagMask);
-                });
+            if (full_vocab || B == 1) {
+                gather(
+                    grid * B, [&](int i) { return xb + (size_t)(i / B) * kLLMaxBatch + i % B; }, kk, 1,
+                    [&](int i, unsigned long long w) {
+                        if (w > kBestTagMask) atomicMax(&sbest_x[i % B], w & ~(unsigned long long)kBestTagMask);
+                    });
+            } else {
+                // pools of several requests: request b's entries lie in the
+                // slices of CTAs b K / seg .. ((b+1) K - 1) / seg, at most `span` of them
+                // (a shorter run repeats its last CTA: a harmless second max).
+                // The CTAs past the pool's end have no entries, but their
+                // (empty) words are read too: every CTA's word of a step is
+                // read by every CTA, which is what keeps any CTA from running
+                // two steps ahead of another (the exchanges' double buffering)
+                const int span = (p.K + p.seg - 1) / p.seg + 1;
+                const int n_cover = (B * p.K + p.seg - 1) / p.seg;
+                gather(
+                    B * span + (grid - n_cover),
+                    [&](int i) {
+                        if (i >= B * span) return xb + (size_t)(n_cover + i - B * span) * kLLMaxBatch;
+                        const int b = i / span;  // b K < B * K <= grid * seg: 32-bit products
+                        const int c_lo = b * p.K / p.seg;
+                        const int c_hi = ((b + 1) * p.K - 1) / p.seg;
+                        return xb + (size_t)min(c_lo + i % span, c_hi) * kLLMaxBatch + b;
+                    },
+                    kk, 1,
+                    [&](int i, unsigned long long w) {
+                        if (i < B * span && w > kBestTagMask)
+                            atomicMax(&sbest_x[i / span], w & ~(unsigned long long)kBestTagMask);
+                    });
+            }
             cons_sync();
             if (tid < B) {
                 const unsigned long long w = sbest_x[tid];
