@@ -879,9 +879,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 }
             }
         }
+        // the requests of the slice (at most nra of them hold a value)
 #pragma unroll
         for (int b = 0; b < MB; ++b) {
             if (b >= B) break;
+            if (b < rb0 || b >= rb0 + nra) continue;
             const unsigned long long w = warp_max_u64(m[b]);
             if (lane == 0 && w) atomicMax(&sbest_c[b], w);
         }
