@@ -236,6 +236,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oGh = take((size_t)kPersistGruGroup * 3 * g.G * sizeof(float));
     const bool pmask = g.max_K > 0 && g.dtype == DOMINO_DTYPE_BF16;
     size_t oM = take(pmask ? (size_t)g.max_B * pool_mask_words(g.V) * 4 : 0);
+    size_t oHs = take(pmask ? (size_t)g.max_B * kPoolHistBins * 4 : 0);
     size_t oC = take(g.max_K > 0 ? (size_t)g.max_B * DOMINO_MAX_VOCAB_PARTITIONS * g.max_K * 4 : 0);
     const bool ll = g.dtype == DOMINO_DTYPE_BF16;  // tagged-exchange persistent driver
     size_t oXa = take(ll ? (size_t)2 * kLLMaxBatch * g.F * 8 : 0);
@@ -272,6 +273,7 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     c->xbest = ll ? (unsigned long long*)(base + oXb) : nullptr;
     c->xg = ll ? (unsigned long long*)(base + oXq) : nullptr;
     c->ghb = ll ? (float*)(base + oGb) : nullptr;
+    c->hist = pmask ? (unsigned*)(base + oHs) : nullptr;
     // zero the small state (a16 padding rows must stay zero for the MMA path)
     if (cudaMemset(base + oH, 0, off - oH) != cudaSuccess || prepare_simt_kernels(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {

@@ -186,6 +186,7 @@ struct domino_ctx {
     unsigned long long* xg;     // [2][3G] tagged hidden-side products of every unit (one request)
     float* gi_table;          // [V, 3G] input-side GRU pre-activations of every token (built at load)
     float* gh_next;           // [kPersistGruGroup][3G] hidden-side pre-activations of the next GRU update (persistent driver)
+    unsigned* hist;           // [max_B, 2048] histogram of the pool scores' top 11 key bits (LM-head epilogue), or null
     float* ghb;               // [2][max_B,3G] hidden-side products W_hh h of the fused per-step launches (bf16 batches), or null
     __nv_bfloat16* wp;        // [4*Gp, G] packed hidden-side GRU weights (bf16 batches), or null
     __nv_bfloat16* h16;       // [2][a_rows, G] bf16 copies of the GRU state (tensor-core operands)

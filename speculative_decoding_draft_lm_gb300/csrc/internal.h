@@ -40,6 +40,8 @@ struct RunArgs {
 };
 
 // SIMT kernels (kernels_simt.cu)
+constexpr int kPoolHistBits = 11;  // first radix digit of the pool select: the top 11 key bits
+constexpr int kPoolHistBins = 1 << kPoolHistBits;
 cudaError_t launch_reset(domino_ctx* c, RunArgs& r);
 cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r);
 cudaError_t launch_first_argmax(domino_ctx* c, RunArgs& r);
@@ -75,7 +77,9 @@ cudaError_t launch_correct_tc(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB,
 
 // cluster radix-select candidate pool (pool.cu)
 bool pool_cluster_supported(const domino_ctx* c);
-cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r);
+// hist: the LM-head epilogue's histogram of the scores' top kPoolHistBits key
+// bits per request, or null (the select then builds its first pass itself)
+cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r, const unsigned* hist);
 cudaError_t launch_pool_cluster_raw(const float* score, int32_t* pool, int B, int V, int K, cudaStream_t st);
 bool pool_cluster_fits(int V);
 // stage C of the tensor-parallel rollout on one GPU: P shard-local top-K, then the merge

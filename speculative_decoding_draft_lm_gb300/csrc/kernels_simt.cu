@@ -20,7 +20,8 @@ inline int grid_for(int items_per_block_unit, int units, int cap) {
 
 // ---------------------------------------------------------------------------
 __global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__ bad, unsigned* __restrict__ sync,
-                        unsigned long long* __restrict__ xbest, int n_keys, int B, int n_xbest) {
+                        unsigned long long* __restrict__ xbest, unsigned* __restrict__ hist, int n_keys, int B,
+                        int n_xbest, int n_hist) {
     pdl_trigger();
     pdl_wait();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -28,6 +29,7 @@ __global__ void k_reset(unsigned long long* __restrict__ keys, int* __restrict__
     if (i < B) bad[i] = 0;
     if (i < 64) sync[i] = 0u;  // grid-barrier counter and the per-step chunk counters
     if (i < n_xbest) xbest[i] = 0ull;  // per-CTA bests of the tagged-exchange driver
+    if (i < n_hist) hist[i] = 0u;      // the pool scores' first-digit histogram
     if (i == 0) sync[kRunEpochWord] += 1u;  // a new tag range for this run's exchange words
 }
 
@@ -434,10 +436,12 @@ __global__ void __launch_bounds__(256) k_backbone_s(const T* __restrict__ hidden
 cudaError_t launch_reset(domino_ctx* c, RunArgs& r) {
     const int n = r.B * kBlock;
     const int nx = c->xbest ? 2 * c->num_sms * kLLMaxBatch : 0;
-    const int m = n > nx ? n : nx;
+    const int nh = c->hist && r.K > 0 ? r.B * kPoolHistBins : 0;
+    int m = n > nx ? n : nx;
+    m = m > nh ? m : nh;
     ++r.launches;
-    return launch_pdl(k_reset, dim3((m + 255) / 256), dim3(256), 0, r.st, c->keys, c->bad, c->sync, c->xbest, n, r.B,
-                      nx);
+    return launch_pdl(k_reset, dim3((m + 255) / 256), dim3(256), 0, r.st, c->keys, c->bad, c->sync, c->xbest, c->hist,
+                      n, r.B, nx, nh);
 }
 
 cudaError_t launch_lmhead_simt(domino_ctx* c, RunArgs& r) {
@@ -486,7 +490,8 @@ cudaError_t launch_pool_select(domino_ctx* c, RunArgs& r, bool score_ready) {
         cudaError_t e = launch_score(c, r);
         if (e != cudaSuccess) return e;
     }
-    if (pool_cluster_supported(c)) return launch_pool_cluster(c, r);
+    // the tensor-core LM-head also histograms the scores' first digit
+    if (pool_cluster_supported(c)) return launch_pool_cluster(c, r, score_ready ? c->hist : nullptr);
     k_pool_select<<<r.B, 1024, 0, r.st>>>(c->score, c->pool, c->cfg.V, r.K);
     DOMINO_LAUNCH_CHECK();
     return cudaSuccess;

@@ -35,6 +35,7 @@ struct EpiLmHead {
     float* L;                  // [B,16,V]
     unsigned long long* keys;  // [B,16], slot 0 = p_1
     float* score;              // [B,V] or null
+    unsigned* hist;            // [B, kPoolHistBins] counts of the scores' top key bits, or null
     __nv_bfloat16* s_out;      // [B,15,F] or null: rows from s_row0 on are W_hid rows
     int V, B, s_row0, F;
     __device__ __forceinline__ void begin(unsigned long long* sb, int t) const {
@@ -61,15 +62,26 @@ struct EpiLmHead {
             return;
         }
         const bool ok = row < V;
+        float m = 0.f;  // the score: max over the 15 used rows
         if (ok) {
             float* dst = L + (size_t)b * kBlock * V + row;
 #pragma unroll
             for (int i = 0; i < kBlock; ++i) dst[(size_t)i * V] = v[i];
             if (score) {
-                float m = v[kRowOffset];
+                m = v[kRowOffset];
 #pragma unroll
                 for (int i = kRowOffset + 1; i < kRowOffset + kProposals; ++i) m = fmaxf(m, v[i]);
                 score[(size_t)b * V + row] = m;
+            }
+        }
+        if (hist) {  // set only with score
+            // the pool select's first radix pass: warp-aggregated counts of the
+            // top key bits (lanes with equal digits add once)
+            const unsigned okm = __ballot_sync(0xffffffffu, ok);
+            if (ok) {
+                const unsigned d = ord_f32(m) >> (32 - kPoolHistBits);
+                const unsigned peers = __match_any_sync(okm, d);
+                if (lane == __ffs(peers) - 1) atomicAdd(&hist[(size_t)b * kPoolHistBins + d], (unsigned)__popc(peers));
             }
         }
         unsigned long long key = ok ? pack_key(v[kRowOffset], (uint32_t)row) : 0ull;
@@ -112,7 +124,8 @@ cudaError_t launch_bn(domino_ctx* c, RunArgs& r, const CUtensorMap& tmB, float* 
     const int tiles = m_tiles * ((N + BN - 1) / BN);
     const int grid = tiles < c->num_sms ? tiles : c->num_sms;
     const int s_row0 = with_s ? v_tiles * tc::kBM : INT_MAX;
-    EpiLmHead epi{c->L, c->keys, score, (__nv_bfloat16*)r.s_out, c->cfg.V, r.B, s_row0, c->cfg.F};
+    EpiLmHead epi{c->L, c->keys, score, score ? c->hist : nullptr, (__nv_bfloat16*)r.s_out, c->cfg.V, r.B, s_row0,
+                  c->cfg.F};
     ++r.launches;
     const int M = with_s ? s_row0 + c->cfg.F : c->cfg.V;
     return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, c->tm_lm_head,

@@ -90,7 +90,8 @@ template <int R>
 __global__ void __launch_bounds__(kPoolThreads, 2) k_pool_cluster(const float* __restrict__ score, long long stride,
                                                                  const int32_t* __restrict__ cand, int shards,
                                                                  int shard_len, int32_t* __restrict__ pool,
-                                                                 int out_stride, int V, int K, int chunk) {
+                                                                 int out_stride, int V, int K, int chunk,
+                                                                 const unsigned* __restrict__ ghist) {
     extern __shared__ __align__(16) uint8_t smem[];
     PoolShared<R>& S = *reinterpret_cast<PoolShared<R>*>(smem);
     unsigned* keys = reinterpret_cast<unsigned*>(smem + sizeof(PoolShared<R>));
@@ -125,8 +126,32 @@ __global__ void __launch_bounds__(kPoolThreads, 2) k_pool_cluster(const float* _
     unsigned prefix = 0, pmask = 0, remaining = (unsigned)Kr;
     const int shifts[3] = {21, 10, 0};
     const int widths[3] = {11, 11, 10};
+    int pass0 = 0;
+    if (ghist) {
+        // the first pass from the counts the LM-head epilogue made (the same
+        // data in every CTA, so each finds the digit without the cluster):
+        // thread t holds bins kBins-1-2t and kBins-2-2t, and a block scan
+        // gives the keys in the bins above them
+        static_assert(kBins == 2 * kPoolThreads && kBins == kPoolHistBins, "two bins per thread");
+        const unsigned* gh = ghist + (size_t)b * kBins;
+        const int t = threadIdx.x;
+        const unsigned c_hi = gh[kBins - 1 - 2 * t], c_lo = gh[kBins - 2 - 2 * t];
+        const unsigned above = block_scan_excl(c_hi + c_lo, S.warp_tot, &S.total);
+        if (above < remaining && above + c_hi >= remaining) {
+            S.digit = (unsigned)(kBins - 1 - 2 * t);
+            S.rem = remaining - above;
+        } else if (above + c_hi < remaining && above + c_hi + c_lo >= remaining) {
+            S.digit = (unsigned)(kBins - 2 - 2 * t);
+            S.rem = remaining - above - c_hi;
+        }
+        __syncthreads();
+        prefix = S.digit << shifts[0];
+        pmask = (unsigned)(kBins - 1) << shifts[0];
+        remaining = S.rem;
+        pass0 = 1;
+    }
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = pass0; pass < 3; ++pass) {
         const int shift = shifts[pass];
         const unsigned nb = 1u << widths[pass];
         const unsigned dmask = nb - 1;
@@ -259,7 +284,7 @@ namespace {
 
 template <int R>
 cudaError_t launch_rows_r(const float* score, long long stride, const int32_t* cand, int shards, int shard_len,
-                          int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st) {
+                          int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st, const unsigned* ghist) {
     const int chunk = (shard_len + R - 1) / R;
     const size_t smem = sizeof(PoolShared<R>) + (size_t)chunk * 4;
     cudaError_t e = cudaFuncSetAttribute(k_pool_cluster<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -281,18 +306,21 @@ cudaError_t launch_rows_r(const float* score, long long stride, const int32_t* c
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_pool_cluster<R>, score, stride, cand, shards, shard_len, pool, out_stride, V, K,
-                              chunk);
+                              chunk, ghist);
 }
 
 // R = 16 for a single row when the GPU has room for it (num_sms = 0: never)
+// ghist: first-digit counts of the rows (direct pool only), or null
 cudaError_t launch_rows(const float* score, long long stride, const int32_t* cand, int shards, int shard_len,
-                        int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st, int num_sms = 0) {
+                        int32_t* pool, int out_stride, int B, int V, int K, cudaStream_t st, int num_sms = 0,
+                        const unsigned* ghist = nullptr) {
     if (num_sms >= kRanksWide && B * shards == 1) {
-        cudaError_t e = launch_rows_r<kRanksWide>(score, stride, cand, shards, shard_len, pool, out_stride, B, V, K, st);
+        cudaError_t e =
+            launch_rows_r<kRanksWide>(score, stride, cand, shards, shard_len, pool, out_stride, B, V, K, st, ghist);
         if (e == cudaSuccess) return e;
         cudaGetLastError();  // wide clusters unavailable: the portable size
     }
-    return launch_rows_r<kRanksPortable>(score, stride, cand, shards, shard_len, pool, out_stride, B, V, K, st);
+    return launch_rows_r<kRanksPortable>(score, stride, cand, shards, shard_len, pool, out_stride, B, V, K, st, ghist);
 }
 
 bool fits(int row_len) {
@@ -311,9 +339,10 @@ bool pool_cluster_fits(int V) { return fits(V); }
 
 bool pool_cluster_supported(const domino_ctx* c) { return fits(c->cfg.V); }
 
-cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r) {
+cudaError_t launch_pool_cluster(domino_ctx* c, RunArgs& r, const unsigned* hist) {
     ++r.launches;
-    return launch_rows(c->score, c->cfg.V, nullptr, 1, c->cfg.V, c->pool, r.K, r.B, c->cfg.V, r.K, r.st, c->num_sms);
+    return launch_rows(c->score, c->cfg.V, nullptr, 1, c->cfg.V, c->pool, r.K, r.B, c->cfg.V, r.K, r.st, c->num_sms,
+                       hist);
 }
 
 bool pool_compact_supported(const domino_ctx* c, int P, int K) {
