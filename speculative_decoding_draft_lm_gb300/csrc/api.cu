@@ -147,8 +147,16 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
     // GRU update and projector layer 1), after the seed update and W_hh h_0.
     // A block of one proposal has no step, but still the seed's second update.
     const bool fused = batch && !gru_tc && r.n_prop >= 2 && step_fused_supported(c, r);
+    // tensor-core batches: per step one joined projector launch (fc1 rows and
+    // W_hh h for the next update), the correction, then an element-wise update
+    const bool joined = gru_tc && c->ghb;
     STEP(DOMINO_PHASE_GRU, GRU(0));
-    STEP(DOMINO_PHASE_GRU, fused ? launch_step_fused(c, r, 0) : GRU(1));
+    if (joined) {
+        STEP(DOMINO_PHASE_GRU, launch_proj_tc(c, r, gm, 0));
+        STEP(DOMINO_PHASE_GRU, launch_update_tc(c, r, 1));
+    } else {
+        STEP(DOMINO_PHASE_GRU, fused ? launch_step_fused(c, r, 0) : GRU(1));
+    }
     {
         // tensor cores once the full-vocabulary correction is a real
         // contraction (two or more requests); CUDA cores for B = 1 and pools
@@ -161,14 +169,14 @@ int run_impl(domino_ctx* c, const void* hidden, const void* s, const int32_t* ve
         }
         const int n_corr = r.n_prop - 1;
         for (int k = 1; k <= n_corr; ++k) {
-            STEP(DOMINO_PHASE_FC1, fused ? launch_step_fused(c, r, k) : FC1(k));
+            STEP(DOMINO_PHASE_FC1, fused ? launch_step_fused(c, r, k) : joined ? launch_proj_tc(c, r, gm, k) : FC1(k));
             if (tc_corr)
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_tc(c, r, tm_a, k));
             else if (r.K > 0 && batch && pool_batch_supported(c))
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_pool_batch(c, r, k));
             else
                 STEP(DOMINO_PHASE_CORRECT, launch_correct_simt(c, r, k));
-            if (k < n_corr && !fused) STEP(DOMINO_PHASE_GRU, GRU(k + 1));
+            if (k < n_corr && !fused) STEP(DOMINO_PHASE_GRU, joined ? launch_update_tc(c, r, k + 1) : GRU(k + 1));
         }
     }
 #undef GRU
@@ -243,7 +251,8 @@ int domino_rollout_init(domino_ctx** out, const domino_config* cfg, int device) 
     size_t oXg = take(ll ? (size_t)2 * kLLMaxBatch * g.G * 8 : 0);
     size_t oXb = take(ll ? (size_t)2 * c->num_sms * kLLMaxBatch * 8 : 0);
     size_t oXq = take(ll ? (size_t)2 * 3 * g.G * 8 : 0);
-    size_t oGb = take(ll ? (size_t)2 * g.max_B * 3 * g.G * sizeof(float) : 0);
+    // hidden-side products of the batched paths: [2][max_B][3G] (fused step) or [2][max_B][4Gp] (packed)
+    size_t oGb = take(ll ? (size_t)2 * g.max_B * 4 * gru_padded_units(g.G) * sizeof(float) : 0);
     c->ws_bytes = off;
     if (cudaMalloc(&c->ws_base, c->ws_bytes) != cudaSuccess) {
         cudaGetLastError();

@@ -161,6 +161,75 @@ struct EpiFc1 {
     }
 };
 
+// Projector layer 1 of step k and the hidden-side GRU products for update
+// k+1 in one contraction of the same state h_k: A = [fc1 (rows 0..F-1, the
+// tile rows past F zero-filled); Wp (packed W_hh rows 4j+q, from row fr
+// on)], B = the bf16 state.  The fc1 rows finish as in EpiFc1; the packed
+// rows are stored raw: W_hh h_k does not depend on the token the correction
+// of step k picks, so only an element-wise update is left after it.
+struct EpiProj {
+    static constexpr int kScratchWords = 1;
+    static constexpr int kL2Ahead = 0;
+    static constexpr int kPfChunk = 16;
+    EpiFc1 fc1;    // rows < fr (k >= 1)
+    float* ghp;    // [B, 4Gp] products of the packed rows
+    int fr, gp4;   // first packed row (a multiple of 128); 4Gp
+    __device__ __forceinline__ void begin(unsigned long long*, int) const {}
+    __device__ __forceinline__ void end(unsigned long long*, int) const {}
+    template <int PF>
+    __device__ __forceinline__ void prefetch(int col0, int row, float* pf) const {
+        if (row < fr) fc1.template prefetch<PF>(col0, row, pf);
+    }
+    __device__ __forceinline__ void operator()(int col0, int row, const float* v, int lane, unsigned long long* sb,
+                                               const float* pf) const {
+        if (row < fr) {  // uniform over the warp: fr is a multiple of 128
+            fc1(col0, row, v, lane, sb, pf);
+            return;
+        }
+        const int pr = row - fr;
+        if (pr >= gp4) return;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int b = col0 + c;
+            if (b < fc1.B) ghp[(size_t)b * gp4 + pr] = v[c];
+        }
+    }
+};
+
+// The update u >= 1 of every unit after the correction that picked its
+// token: h = GRU(T[p_u], W_hh h_{u-1}, h_{u-1}) from the token-table row,
+// the packed products of the projector launch and the previous state.
+__global__ void __launch_bounds__(256) k_gru_update(const float* __restrict__ gi_table, const float* __restrict__ ghp,
+                                                    const float* __restrict__ h_in, float* __restrict__ h_out,
+                                                    __nv_bfloat16* __restrict__ h16_out,
+                                                    const unsigned long long* __restrict__ keys,
+                                                    const int32_t* __restrict__ forced, int* __restrict__ bad,
+                                                    int* __restrict__ err, float* __restrict__ dbg_h, int u, int B,
+                                                    int G, int gp4, int V) {
+    pdl_trigger();
+    pdl_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= B * G) return;
+    const int b = i / G, j = i - b * G;
+    int t = forced ? forced[(size_t)b * kProposals + (u - 1)] : (int)key_index(keys[(size_t)b * kBlock + (u - 1)]);
+    if (t < 0 || t >= V) {
+        if (j == 0) {
+            bad[b] = 1;
+            atomicOr(err, kErrBadToken);
+        }
+        t = 0;
+    }
+    const float* gi = gi_table + (size_t)t * 3 * G + j;
+    const float4 gh = *reinterpret_cast<const float4*>(ghp + (size_t)b * gp4 + 4 * j);  // r, z, n, 0
+    const float r = sigmoidf_(__ldg(gi) + gh.x);
+    const float z = sigmoidf_(__ldg(gi + G) + gh.y);
+    const float n = tanhf(__ldg(gi + 2 * G) + r * gh.z);
+    const float h = (1.f - z) * n + z * h_in[(size_t)b * G + j];
+    h_out[(size_t)b * G + j] = h;
+    h16_out[(size_t)b * G + j] = __float2bfloat16_rn(h);
+    if (dbg_h) dbg_h[((size_t)b * kProposals + u) * G + j] = h;
+}
+
 template <int BN, class Epi>
 cudaError_t launch_gemm(domino_ctx* c, RunArgs& r, const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int K,
                         const Epi& epi) {
@@ -178,6 +247,26 @@ cudaError_t launch_gemm(domino_ctx* c, RunArgs& r, const CUtensorMap& tmA, const
     ++r.launches;
     return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, tmA, tmA, tmB, M, INT_MAX, r.B, K, epi,
                       c->err);
+}
+
+// two A matrices: tiles m < m_split from tmA, the rest from tmA2
+template <int BN, class Epi>
+cudaError_t launch_gemm2(domino_ctx* c, RunArgs& r, const CUtensorMap& tmA, const CUtensorMap& tmA2,
+                         const CUtensorMap& tmB, int M, int m_split, int K, const Epi& epi) {
+    using S = tc::GemmShape<BN, Epi::kScratchWords>;
+    static bool attr_set[64] = {};
+    auto kern = tc::k_gemm_tc<BN, Epi>;
+    const int slot = c->device & 63;
+    if (!attr_set[slot]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[slot] = true;
+    }
+    const int tiles = ((M + tc::kBM - 1) / tc::kBM) * ((r.B + BN - 1) / BN);
+    const int grid = tiles < c->num_sms ? tiles : c->num_sms;
+    ++r.launches;
+    return launch_pdl(kern, dim3(grid), dim3(tc::kGemmThreads), S::SMEM, r.st, tmA, tmA2, tmB, M, m_split, r.B, K,
+                      epi, c->err);
 }
 
 // 16 requests per tile for both contractions: their A matrices are small
@@ -225,6 +314,9 @@ cudaError_t prepare_gru_tc(domino_ctx* c, RunArgs& r, GruMaps* m) {
         cudaError_t e = make_tmap_bf16(&m->h[i], c->h16 + (size_t)i * c->a_rows * g.G, (uint64_t)c->a_rows,
                                        (uint64_t)g.G, bn);
         if (e != cudaSuccess) return e;
+        e = make_tmap_bf16(&m->h32[i], c->h16 + (size_t)i * c->a_rows * g.G, (uint64_t)c->a_rows, (uint64_t)g.G,
+                           32u);
+        if (e != cudaSuccess) return e;
     }
     return make_tmap_bf16(&m->fc1, c->fc1, (uint64_t)g.F, (uint64_t)g.G, (uint32_t)tc::kBM);
 }
@@ -238,6 +330,42 @@ cudaError_t launch_gru_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int u) {
     EpiGru epi{c->gi_table, h_in, h_out, h16_out, (const unsigned long long*)c->keys, r.forced, c->bad, c->err,
                r.dbg.h, r.B, g.G, g.V, u};
     return launch_any_bn(c, r, c->tm_wp, m.h[(u - 1) & 1], 4 * gru_padded_units(g.G), g.G, epi);
+}
+
+// Launch k of the joined projector: k >= 1 projects h_k (fc1 rows), and
+// unless k is the last step (or k = 0, the seed state alone) also forms the
+// packed products W_hh h_k into GHP[k & 1] for update k+1.
+cudaError_t launch_proj_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int k) {
+    const domino_config& g = c->cfg;
+    const int n_corr = r.n_prop - 1;
+    const int gp4 = 4 * gru_padded_units(g.G);
+    const bool gh = k < n_corr || k == 0;
+    const int fr = k > 0 ? (g.F + tc::kBM - 1) / tc::kBM * tc::kBM : 0;
+    EpiProj epi{EpiFc1{(const __nv_bfloat16*)r.s, c->a, c->a16, r.dbg.z, r.B, g.F, k},
+                c->ghb + (size_t)(k & 1) * g.max_B * gp4, fr, gh ? gp4 : 0};
+    const int M = fr + (gh ? gp4 : 0);
+    const int m_split = fr / tc::kBM;
+    // 16 requests per tile while the tiles fit one wave, else 32
+    const int tiles16 = ((M + tc::kBM - 1) / tc::kBM) * ((r.B + 15) / 16);
+    if (tiles16 <= c->num_sms)
+        return launch_gemm2<16>(c, r, m.fc1, c->tm_wp, m.h[k & 1], M, m_split, g.G, epi);
+    return launch_gemm2<32>(c, r, m.fc1, c->tm_wp, m.h32[k & 1], M, m_split, g.G, epi);
+}
+
+// Update u >= 1 after the correction of step u - 1 (token p_u): the packed
+// products come from projector launch u - 1.
+cudaError_t launch_update_tc(domino_ctx* c, RunArgs& r, int u) {
+    const domino_config& g = c->cfg;
+    const int gp4 = 4 * gru_padded_units(g.G);
+    const float* ghp = c->ghb + (size_t)((u - 1) & 1) * g.max_B * gp4;
+    const float* h_in = c->h + (size_t)h_slot(u - 1) * g.max_B * g.G;
+    float* h_out = c->h + (size_t)h_slot(u) * g.max_B * g.G;
+    __nv_bfloat16* h16_out = c->h16 + (size_t)(u & 1) * c->a_rows * g.G;
+    const int n = r.B * g.G;
+    ++r.launches;
+    return launch_pdl(k_gru_update, dim3((n + 255) / 256), dim3(256), 0, r.st, (const float*)c->gi_table, ghp, h_in,
+                      h_out, h16_out, (const unsigned long long*)c->keys, r.forced, c->bad, c->err, r.dbg.h, u, r.B,
+                      g.G, gp4, g.V);
 }
 
 cudaError_t launch_fc1_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int k) {

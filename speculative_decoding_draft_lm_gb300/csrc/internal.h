@@ -104,7 +104,8 @@ cudaError_t build_gi_table(domino_ctx* c, cudaStream_t st);
 
 // tcgen05 GRU update and projector layer 1 for batches (gru_tc.cu)
 struct GruMaps {
-    CUtensorMap h[2];  // the bf16 state copies H16[0], H16[1] (B operand of both contractions)
+    CUtensorMap h[2];    // the bf16 state copies H16[0], H16[1] (B operand of both contractions), 16-row boxes
+    CUtensorMap h32[2];  // the same with 32-row boxes (32-column tiles of the joined projector)
     CUtensorMap fc1;
 };
 int gru_padded_units(int G);
@@ -114,6 +115,10 @@ cudaError_t pack_gru_weights(domino_ctx* c, cudaStream_t st);
 cudaError_t prepare_gru_tc(domino_ctx* c, RunArgs& r, GruMaps* m);
 cudaError_t launch_gru_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int u);
 cudaError_t launch_fc1_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int k);
+// the joined projector (fc1 rows of step k with the packed W_hh products for
+// update k+1) and the element-wise update after the correction (gru_tc.cu)
+cudaError_t launch_proj_tc(domino_ctx* c, RunArgs& r, const GruMaps& m, int k);
+cudaError_t launch_update_tc(domino_ctx* c, RunArgs& r, int u);
 
 // persistent driver of the GRU seed and the 14 corrected steps (persist.cu).
 // Requests per GRU/projector staging group; the workspace's hidden-side
