@@ -33,18 +33,24 @@
 // loads several words at once and reads the ones without the tag again
 // together, so a late word costs one more L2 round trip, not one per word.
 //
-// Dot products use a lane layout without shared-memory bank conflicts: lane
-// l holds elements 128c + 4l .. 128c + 4l + 3 of a row or vector.  A warp
-// keeps up to two weight rows in registers, streams every request's state
-// through 16-byte shared loads, and reduces all its (row, request) dots in
-// one transposed butterfly.  The fc1 rows of a CTA, and for pools its W_hh
-// rows and pool rows (as many as fit), stay in shared memory for the whole
-// launch.  Over the full
-// vocabulary a producer warp streams fc2 with bulk copies into a ring
-// (walking the slice in alternating directions so a step starts on the rows
-// the last one read); the last seventh of every slice is shared: producers
-// that finish their own part early claim those chunks through a per-step
-// counter, which absorbs the per-step spread of the CTAs' streaming rates.
+// The fc1 rows of a CTA, and for pools its W_hh rows (and its pool rows
+// when they fit), stay in shared memory for the whole launch.  With all its
+// rows resident, a CTA's projector runs on the tensor cores (16-row tiles,
+// one column per request, the fp32 state split into bf16 leading parts and
+// remainders); over the full vocabulary, where W_hh is read from L2, a warp
+// keeps two rows in registers and streams the state from shared memory in a
+// lane layout without bank conflicts (lane l holds elements 128c + 4l ..
+// 128c + 4l + 3), reducing all its (row, request) dots in one transposed
+// butterfly.  Over the full vocabulary a producer warp streams fc2 with bulk
+// copies into a ring (walking the slice in alternating directions so a step
+// starts on the rows the last one read); the last seventh of every slice is
+// shared: producers that finish their own part early claim those chunks
+// through a per-step counter, which absorbs the per-step spread of the CTAs'
+// streaming rates.  Pool rows that do not fit are gathered through the ring
+// step by step, with a fixed chunk count per step.  A pool CTA reads only the
+// activations of the requests its slice covers, and with several requests
+// the bests only of the CTAs that cover each request (and of those past the
+// pool's end, so that every CTA's word is still read by all).
 //
 // Every wait (exchange word, ring slot) is bounded; on a timeout the kernel
 // raises the device error word, and all consumer warps leave together (the
