@@ -102,9 +102,11 @@ struct LLParams {
 
 struct LLLayout {
     int ring, bars, srow, swhh, sfc1, sh, spart, sa, sL, sbias, spid, sqid, ss, sgh, sgall, sred, stok, misc, total;
-    // ra: requests whose activations a CTA keeps (those its correction slice covers)
+    // ra: requests whose activations a CTA keeps (those its correction slice covers);
+    // wh_res: W_hh rows resident, which is the case exactly for pools
     __host__ __device__ LLLayout(int n_slots, int slot_bytes, int G, int F, int jpc, int fpc, int seg, int B, int ra,
                                  bool wh_res) {
+        const bool pools = wh_res;
         auto up = [](int x) { return (x + 127) & ~127; };
         const int rs = G + kPad;                       // row stride of the resident rows and of the state
         const int mt = (fpc + 3 * jpc + 15) / 16;      // 16-row tiles of the tensor-core projector
@@ -119,8 +121,8 @@ struct LLLayout {
         sa = o;    o = up(o + 4 * ra * F);
         sL = o;    o = up(o + 4 * seg);
         sbias = o; o = up(o + 4 * seg);
-        spid = o;  o = up(o + 4 * seg);                   // pool ids of the slice
-        sqid = o;  o = up(o + 4 * seg);                   // the same, for the producer warp
+        spid = o;  o = up(o + (pools ? 4 * seg : 0));     // pool ids of the slice
+        sqid = o;  o = up(o + (pools ? 4 * seg : 0));     // the same, for the producer warp
         ss = o;    o = up(o + 4 * B * kProposals * fpc);  // s entries of the CTA's projector outputs
         sgh = o;   o = up(o + 4 * B * 3 * jpc);           // hidden-side products of the CTA's units
         sgall = o; o = up(o + (B == 1 ? 4 * 3 * G : 0));  // one request: those of every unit
