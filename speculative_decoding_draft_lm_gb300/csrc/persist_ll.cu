@@ -833,9 +833,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         unsigned long long m[MB];  // this lane's best per request of the rows it finishes
 #pragma unroll
         for (int b = 0; b < MB; ++b) m[b] = 0ull;
+        // a small resident slice (at most two rows per warp): one row per warp
+        // at a time, so that every warp shares the dot products
+        const bool row_mode = p.resident && nw <= 2 * kConsumerWarps;
+        if (row_mode) {
+            for (int rr = warp; rr < nw; rr += kConsumerWarps) {
+                const int slot = rr / kRows;
+                if (k == 1 && !tc::mbar_wait(full0 + 8 * slot, 0u, abort_flag, p.err)) {
+                    failed = true;
+                    break;
+                }
+                const int item = (int)w0 + rr;
+                const int b = item / p.K;
+                if (b != areg_b) load_areg(b);
+                const __nv_bfloat16* row =
+                    reinterpret_cast<const __nv_bfloat16*>(ring + (size_t)slot * slot_bytes) + (size_t)(rr % kRows) * F;
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < NCH; ++cc) {
+                    const int e = (lane + 32 * cc) * 8;
+                    if (e < F) {
+                        float wv[8];
+                        lds8(row + e, wv);
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) {
+                            a0 = fmaf(wv[i], areg[cc][i], a0);
+                            a1 = fmaf(wv[i + 1], areg[cc][i + 1], a1);
+                        }
+                    }
+                }
+                float tot = a0 + a1;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+                if (lane == 0) {
+                    const int v = spid[rr];
+                    const float cv = tot + sbias[rr] + sL[rr];
+                    const unsigned long long key = best_key(cv, v);
+#pragma unroll
+                    for (int bb = 0; bb < MB; ++bb)
+                        if (bb == b) m[bb] = max(m[bb], key);
+                    if (p.dbg_scores) p.dbg_scores[((size_t)b * kCorrected + (k - 1)) * p.K + item % p.K] = cv;
+                }
+            }
+        }
         // one loop for both layouts (a single copy of the slot code): resident
         // pool rows, chunk c in slot c; or ring slots, slot q for warp q % n_cons
-        {
+        if (!row_mode) {
             int c_res = warp;
             const bool active = p.resident ? true : warp < p.n_cons;
             while (active) {
