@@ -391,15 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
     };
 
     // ---- projector items of this CTA: its fc1 rows (item < fn, k > 0) and
-    // its units' W_hh rows (item >= fn, when gh is set).  A warp takes one
-    // item, or two consecutive items, with the rows in registers, forms the
-    // lane-partial dots with every request's state (streamed from shared
-    // memory once per chunk for both rows), reduces all of them in one
-    // transposed butterfly, and finishes them on as many lanes at once.
-    // This path serves the rows read from L2 (the W_hh rows over the full
-    // vocabulary): one pass of pairs requests them as early as possible,
-    // while other warps take the fc1 pairs.
-    // xg_k: where the hidden-side products are published as well (one request), or null
+    // its units' W_hh rows (item >= fn, when gh is set).  With all of them
+    // resident (pools) they run on the tensor cores (tc_pass).  Otherwise
+    // (the full vocabulary, W_hh rows read from L2) a warp takes two
+    // consecutive items with the rows in registers, forms the lane-partial
+    // dots with every request's state (streamed from shared memory once per
+    // chunk for both rows), reduces all of them in one transposed butterfly
+    // and finishes them on as many lanes at once; the fc1 pairs run on warps
+    // of their own, the W_hh pairs (requested as early as possible) on the
+    // others.  xg_k: where the hidden-side products are published as well
+    // (one request), or null.
     auto project = [&](int k, bool gh, bool pub_a, unsigned tag_a, unsigned long long* xa_k, unsigned long long* xg_k) {
         const int nf = k > 0 ? fn : 0;
         const int n_items = nf + (gh ? 3 * jn : 0);
@@ -553,10 +554,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
             if (p.dbg_h) p.dbg_h[((size_t)b * kProposals + u) * G + j] = h;
         }
     };
-    // ---- `count` tagged words, word i at addr(i): four loads per thread
-    // in flight (eight for more than four requests); the words that do not carry the tag yet are read again
-    // together (one L2 round trip per retry round for all of them), with a
-    // short back-off between rounds; bounded.  consume(i, word) for each.
+    // ---- `count` tagged words, word i at addr(i): four loads per thread in
+    // flight (eight for more than four requests); the words that do not carry
+    // the tag yet are read again together (one L2 round trip per retry round
+    // for all of them), with a short back-off between rounds; bounded.
+    // consume(i, word) for each.
     auto gather = [&](int count, auto addr, unsigned tag, int mode, auto consume) {
         constexpr int kNT = kConsumerWarps * 32, kDepth = MB > 4 ? 8 : 4;
         for (int base = 0; base < count; base += kDepth * kNT) {
