@@ -256,11 +256,26 @@ __global__ void __launch_bounds__(kPoolThreads, 2) k_pool_cluster(const float* _
         S.eq = eq_cta;
     }
     cluster.sync();
-    unsigned gt_before_r = 0, eq_before_r = 0;
-    for (int r = 0; r < rank; ++r) {
-        gt_before_r += *cluster.map_shared_rank(&S.gt, r);
-        eq_before_r += *cluster.map_shared_rank(&S.eq, r);
+    // the counts of the CTAs before this one: one warp reads them in parallel
+    // (lane r from rank r) and sums them, instead of a chain of remote reads
+    if (threadIdx.x < 32) {
+        unsigned g = 0, e = 0;
+        if (lane < rank) {
+            g = *cluster.map_shared_rank(&S.gt, lane);
+            e = *cluster.map_shared_rank(&S.eq, lane);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (lane == 0) {
+            S.digit = g;  // the selection's scratch words are free again: reused for the sums
+            S.rem = e;
+        }
     }
+    __syncthreads();
+    const unsigned gt_before_r = S.digit, eq_before_r = S.rem;
     const unsigned eq_before = eq_before_r + eq_before_t;
     const unsigned eq_take = eq_before >= need ? 0u : min(eq, need - eq_before);
     // ids written before this thread: all greater ones, and the equal ones taken so far
