@@ -69,6 +69,7 @@ namespace {
 constexpr int kRows = 4;           // fc2 rows per ring slot
 constexpr int kMaxSlots = 64;
 constexpr int kShareDiv = 7;       // a seventh of each full-vocabulary slice is shared
+constexpr int kKeepTenths = 4;     // last 4/10 of a full-vocabulary walk: normal L2 priority
 constexpr int kProducerLanes = 4;  // lanes of the producer warp that issue copies
 constexpr int kMaxSeg = 2048;
 constexpr int kPad = 8;            // elements after each resident row and each state row (bank spread)
@@ -225,6 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
         if (lane >= kProducerLanes) return;
         constexpr unsigned kLanes = (1u << kProducerLanes) - 1u;
         const uint64_t pol = full_vocab ? tc::policy_evict_normal() : tc::policy_evict_last();
+        // Full vocabulary: the walk reverses every step, so the rows a step reads
+        // last are the next step's first. The walk's head is loaded evict-first
+        // and its last kKeepTenths/10 (the shared tails included) at normal
+        // priority, so that the head's misses evict one another rather than the
+        // tail a slower CTA has yet to re-read (B=1 K0: 883.7 -> 877.6 us per block).
+        const uint64_t pol_head = tc::policy_evict_first();
+        const int n_head = n_static - max(0, (kKeepTenths * n_chunks + 5) / 10 - n_share);
+        uint64_t pol_fc2 = pol;
         int q = 0;        // slots issued so far (same in every lane)
         bool ok = true;   // same in every lane
         // fill slot number qq with rows/entries [item0, item0 + nr); item0 < 0: end of a step
@@ -239,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 const uint32_t dst = tc::smem_u32(ring + (size_t)slot * slot_bytes);
                 tc::mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)(nr * row_bytes));
                 if (full_vocab) {
-                    tc::bulk_load(dst, p.fc2 + (size_t)item0 * F, (uint32_t)(nr * row_bytes), full0 + 8 * slot, pol);
+                    tc::bulk_load(dst, p.fc2 + (size_t)item0 * F, (uint32_t)(nr * row_bytes), full0 + 8 * slot, pol_fc2);
                 } else {
                     for (int r = 0; r < nr; ++r)
                         tc::bulk_load(dst + (uint32_t)(r * row_bytes), p.fc2 + (size_t)sqid[item0 - w0 + r] * F,
@@ -282,12 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_rollout_ll(LLParams p) {
                 for (int ci0 = 0; ci0 < n_static && ok; ci0 += kProducerLanes) {
                     const int ci = ci0 + lane;
                     const int c = fwd ? ci : n_chunks - 1 - ci;
+                    pol_fc2 = ci < n_head ? pol_head : pol;
                     round(ci < n_static, w0 + c * kRows, min(kRows, nw - c * kRows));
                 }
                 if (full_vocab && ok) {
                     // shared tails of every slice, kProducerLanes chunks per claim;
                     // the counters are cleared by the run's first kernel
                     if (k == 1) pdl_wait();
+                    pol_fc2 = pol;
                     unsigned* ctr = p.claim + k;
                     unsigned base = lane == 0 ? atomicAdd(ctr, (unsigned)kProducerLanes) : 0u;
                     base = __shfl_sync(kLanes, base, 0);
