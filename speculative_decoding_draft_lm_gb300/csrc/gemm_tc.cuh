@@ -28,9 +28,13 @@
 //
 // Tiles are visited m-major (tile t -> m = t / n_tiles, n = t % n_tiles), grid
 // stride over a persistent grid of one CTA per SM, so CTAs that share an A
-// tile run at the same time.  Every wait is bounded (tc::mbar_wait); on a
-// timeout the block drains its copies and MMAs, frees TMEM and returns with
-// the device error word set.
+// tile run at the same time.  An Epi with a `rev` member set walks the m tiles
+// in reverse (m = m_tiles - 1 - t / n_tiles); one with a kKeepTenths constant
+// loads the A tiles of the last kKeepTenths/10 of its walk at normal L2
+// priority instead of evict-first.  A launch per step over the same A that
+// alternates `rev` then finds in L2 the tiles the previous launch read last.
+// Every wait is bounded (tc::mbar_wait); on a timeout the block drains its
+// copies and MMAs, frees TMEM and returns with the device error word set.
 #pragma once
 
 #include "tc_common.cuh"
@@ -47,6 +51,24 @@ constexpr int kEpiScratch = 256;  // 64-bit words
 constexpr int kPrefetch = 64;     // per-thread epilogue prefetch registers
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+
+// optional Epi members: `rev` (reversed m-tile walk) and kKeepTenths (see above)
+template <class E>
+__device__ __forceinline__ auto tile_rev(const E& e, int) -> decltype(bool(e.rev)) {
+    return e.rev;
+}
+template <class E>
+__device__ __forceinline__ bool tile_rev(const E&, long) {
+    return false;
+}
+template <class E>
+__device__ __forceinline__ auto tile_keep(const E&, int) -> decltype(int(E::kKeepTenths)) {
+    return E::kKeepTenths;
+}
+template <class E>
+__device__ __forceinline__ int tile_keep(const E&, long) {
+    return 0;
+}
 
 template <int BN, int SCRATCH_WORDS = kEpiScratch>
 struct GemmShape {
@@ -116,16 +138,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int k_iters = (K + kBK - 1) / kBK;
     const int tiles = m_tiles * n_tiles;
     int issued = 0;
+    const bool rev = tile_rev(epi, 0);
+    auto m_of = [&](int t) {
+        const int m = t / n_tiles;
+        return rev ? m_tiles - 1 - m : m;
+    };
+    const int t_keep = tiles - (tile_keep(epi, 0) * tiles + 5) / 10;  // tiles t >= t_keep: normal priority
 
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_first();
+            const uint64_t pol_a_keep = policy_evict_normal();
             const uint64_t pol_b = policy_evict_last();
             const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
             const int total = my_tiles * k_iters;
             const int pre = total < S::STAGES ? total : S::STAGES;  // chunk i sits in stage i
             auto a_row = [&](int t, const CUtensorMap*& ta) {
-                const int m = t / n_tiles;
+                const int m = m_of(t);
                 const bool second = m >= m_split;
                 ta = second ? &tmA2 : &tmA;
                 return (second ? m - m_split : m) * kBM;
@@ -135,7 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const CUtensorMap* ta;
                 const int arow = a_row(t, ta);
                 mbar_arrive_expect_tx(full0 + 8 * i, S::STAGE);
-                tma_load_2d(smem_u32(smem + (size_t)i * S::STAGE), ta, kk * kBK, arow, full0 + 8 * i, pol_a);
+                tma_load_2d(smem_u32(smem + (size_t)i * S::STAGE), ta, kk * kBK, arow, full0 + 8 * i,
+                            t >= t_keep ? pol_a_keep : pol_a);
             }
             if (Epi::kL2Ahead > 0) {
                 const uint64_t pol_l2 = policy_evict_normal();
@@ -162,7 +192,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (i >= pre) {
                         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, err)) break;
                         mbar_arrive_expect_tx(full0 + 8 * stage, S::STAGE);
-                        tma_load_2d(sa, ta, kk * kBK, arow, full0 + 8 * stage, pol_a);
+                        tma_load_2d(sa, ta, kk * kBK, arow, full0 + 8 * stage, t >= t_keep ? pol_a_keep : pol_a);
                     }
                     tma_load_2d(sa + S::A_BYTES, &tmB, kk * kBK, n * BN, full0 + 8 * stage, pol_b);
                     ++issued;
@@ -241,12 +271,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float pf[PF];
         if ((int)blockIdx.x < tiles && c_lo < c_hi) {
             const int t0 = blockIdx.x;
-            epi.template prefetch<PF>((t0 % n_tiles) * BN + 16 * c_lo, (t0 / n_tiles) * kBM + quarter * 32 + lane, pf);
+            epi.template prefetch<PF>((t0 % n_tiles) * BN + 16 * c_lo, m_of(t0) * kBM + quarter * 32 + lane, pf);
         }
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, err)) break;
             tc_fence_after();
-            const int m = t / n_tiles, n = t % n_tiles;
+            const int m = m_of(t), n = t % n_tiles;
             const int row = m * kBM + quarter * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll
@@ -260,7 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             const int tn = t + gridDim.x;  // the next tile's epilogue inputs, during its MMAs
             if (tn < tiles && c_lo < c_hi)
-                epi.template prefetch<PF>((tn % n_tiles) * BN + 16 * c_lo, (tn / n_tiles) * kBM + quarter * 32 + lane,
+                epi.template prefetch<PF>((tn % n_tiles) * BN + 16 * c_lo, m_of(tn) * kBM + quarter * 32 + lane,
                                           pf);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
